@@ -1,0 +1,430 @@
+/*
+ * pkm_oracle.c -- plain, slow, single-threaded CPU oracle for the paged-KV MLA hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, includes or calls
+ * this file; only the tests, the package's smoke check and the benchmark's CPU-baseline
+ * leg load it.  It shares no code, header, table or constant with the CUDA path.
+ *
+ * What it computes, and from which passage:
+ *   - generic_flare_mla_decompress_k_cache_ragged_paged (Modular MAX kernels,
+ *     nn/kv_cache_ragged), description and Args: for every request b, the rows
+ *     [buffer_row_offsets[b], buffer_row_offsets[b+1]) of the ragged buffer receive the
+ *     latent K vectors of cache tokens starting at cache_offsets[b]; the gathered rows go
+ *     to k_latent_buffer, and k_buffer = latent[:, :kv_lora_rank] x weight^T.
+ *   - mla_prefill_decode_graph_fp8 (Modular MAX kernels, attention/gpu/mla_graph),
+ *     Parameters (m/n/k_scale_granularity) and Args (w_k, w_k_scale,
+ *     buffer_row_offsets, cache_offsets, buffer_length): the same decompress with an
+ *     e4m3 weight carrying block scales; the activations are quantised per token per
+ *     128-column block (the reading of the silent points is stated at each function).
+ *   - kv_matmul_ragged_paged (Modular MAX kernels, nn/kv_cache_ragged), Args: a GEMM on
+ *     the ragged hidden_state whose rows are written into the paged cache of one layer,
+ *     after each request's existing cache length.
+ *
+ * Arithmetic: fp64 accumulation; the only roundings are the final fp64 -> bf16
+ * round-to-nearest-even, and (FP8 path) the activation quantisation, which is taken in
+ * fp32 exactly as the GPU takes it (a quantised code is an integer decision, so both
+ * sides decide it in the same precision).
+ *
+ * Number formats are written from their definitions:
+ *   bf16  = 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits (IEEE-754 binary32
+ *           truncated to its upper 16 bits);
+ *   e4m3  = the OCP FP8 "E4M3" format: 1 sign, 4 exponent bits (bias 7), 3 fraction bits,
+ *           no infinities, S.1111.111 is NaN, largest finite 448, smallest subnormal 2^-9.
+ *
+ * Every pointer is host memory owned by the caller.  Functions return 0 on success and a
+ * positive code when the metadata points outside the cache (see each function).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------------------ */
+/* bf16                                                                                  */
+/* ------------------------------------------------------------------------------------ */
+
+/* Exact value of a bf16 bit pattern (every bf16 is a float whose low 16 bits are zero). */
+double oracle_bf16_to_double(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round-half-to-even of a non-negative double k to an integer-valued double. */
+static double rne_integer(double k) {
+    double fl = floor(k);
+    double frac = k - fl; /* exact: k and fl share the exponent range */
+    if (frac > 0.5) return fl + 1.0;
+    if (frac < 0.5) return fl;
+    return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+/* fp64 -> bf16, round to nearest, ties to even, overflow to infinity, directly from the
+ * double (no intermediate float rounding).  bf16 keeps 8 significant bits; its smallest
+ * normal is 2^-126 and its subnormal quantum is 2^-133. */
+uint16_t oracle_double_to_bf16(double x) {
+    if (isnan(x)) return 0x7FC0;
+    uint16_t sign = signbit(x) ? 0x8000 : 0x0000;
+    double a = fabs(x);
+    if (isinf(a)) return sign | 0x7F80;
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);                 /* a = m * 2^e, m in [0.5, 1) */
+    int qexp = e - 8;             /* 8 significant bits */
+    if (qexp < -133) qexp = -133; /* subnormal quantum */
+    double quantum = ldexp(1.0, qexp);
+    double r = rne_integer(a / quantum) * quantum; /* a / quantum is exact */
+    if (r >= ldexp(1.0, 128)) return sign | 0x7F80;
+    float f = (float)r; /* exact: r has at most 8 significant bits and is in range */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return sign | (uint16_t)(u >> 16);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* e4m3 (OCP FP8 E4M3, "fn" variant: finite values and NaN only)                         */
+/* ------------------------------------------------------------------------------------ */
+
+double oracle_e4m3_to_double(uint8_t q) {
+    int s = (q >> 7) & 1;
+    int e = (q >> 3) & 0xF;
+    int m = q & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);            /* subnormal: 0.m x 2^(1-7) */
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);   /* normal: 1.m x 2^(e-7) */
+    return s ? -v : v;
+}
+
+/* float -> e4m3 with round-to-nearest-even and saturation to the largest finite value
+ * (448).  NaN maps to the positive NaN code 0x7F.  The sign of zero is kept.  The result
+ * is found by rounding |x| on the e4m3 grid (4 significant bits, subnormal quantum 2^-9)
+ * and looking the rounded value up among the 127 finite non-negative codes. */
+uint8_t oracle_float_to_e4m3_satfinite(float x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E; /* saturate (also covers +-inf) */
+    double r = 0.0;
+    if (a != 0.0) {
+        int e;
+        frexp(a, &e);              /* a = m * 2^e, m in [0.5, 1) */
+        int qexp = e - 4;          /* 4 significant bits */
+        if (qexp < -9) qexp = -9;  /* subnormal quantum */
+        double quantum = ldexp(1.0, qexp);
+        r = rne_integer(a / quantum) * quantum;
+    }
+    /* r <= 448 here: the largest value below 448 rounds at most up to 448 */
+    for (int code = 0; code <= 0x7E; ++code)
+        if (oracle_e4m3_to_double((uint8_t)code) == r) return sign | (uint8_t)code;
+    return 0x7F; /* unreachable for finite input */
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Paged-cache addressing                                                                */
+/* ------------------------------------------------------------------------------------ */
+
+/* Element offset (from the start of `layer`'s cache) of token t of request b:
+ * logical page t / page_size through the page table, slot t % page_size.
+ * Returns -1 if the logical page is past the table row or the physical page is past the
+ * cache. */
+static int64_t token_offset(const uint32_t* page_table, int32_t max_pages_per_seq,
+                            int32_t num_pages, int32_t page_size, int64_t page_stride,
+                            int64_t slot_stride, int32_t b, uint64_t t) {
+    uint64_t logical_page = t / (uint64_t)page_size;
+    uint64_t slot = t % (uint64_t)page_size;
+    if (logical_page >= (uint64_t)max_pages_per_seq) return -1;
+    uint32_t page = page_table[(int64_t)b * max_pages_per_seq + (int64_t)logical_page];
+    if (page >= (uint32_t)num_pages) return -1;
+    return (int64_t)page * page_stride + (int64_t)slot * slot_stride;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* generic_flare_mla_decompress_k_cache_ragged_paged (bf16)                              */
+/* ------------------------------------------------------------------------------------ */
+
+/*
+ * Step 1 (gather), the explicit loop of the description: for each request b and each
+ * i in [0, bro[b+1] - bro[b]): row r = bro[b] + i, cache token t = co[b] + i;
+ * k_latent[r, 0:C] = cache[layer][page(b, t)][slot(t)][0:C], copied bit for bit.
+ * Rows r >= buffer_length are not written (buffer_length is the row count of the
+ * outputs); rows not covered by any request are not written either.
+ * row_written[r] (optional, length buffer_length) is set to 1 for every written row.
+ * Returns 0, or 4 if some token resolved outside the page table / the cache (that row is
+ * then skipped).
+ */
+int oracle_gather_latent(const uint16_t* cache, int64_t layer_stride, int64_t page_stride,
+                         int64_t slot_stride, int32_t num_pages, int32_t page_size,
+                         const uint32_t* page_table, int32_t max_pages_per_seq,
+                         uint32_t layer_idx, const uint32_t* buffer_row_offsets,
+                         const uint32_t* cache_offsets, int32_t batch,
+                         int32_t buffer_length, int32_t latent_cols, uint16_t* k_latent,
+                         uint8_t* row_written) {
+    int status = 0;
+    const uint16_t* layer = cache + (int64_t)layer_idx * layer_stride;
+    for (int32_t b = 0; b < batch; ++b) {
+        uint32_t begin = buffer_row_offsets[b];
+        uint32_t end = buffer_row_offsets[b + 1];
+        for (uint32_t i = 0; begin + i < end; ++i) {
+            uint64_t r = (uint64_t)begin + i;
+            if (r >= (uint64_t)buffer_length) break;
+            uint64_t t = (uint64_t)cache_offsets[b] + i;
+            int64_t off = token_offset(page_table, max_pages_per_seq, num_pages, page_size,
+                                       page_stride, slot_stride, b, t);
+            if (off < 0) {
+                status = 4;
+                continue;
+            }
+            memcpy(k_latent + r * (uint64_t)latent_cols, layer + off,
+                   sizeof(uint16_t) * (size_t)latent_cols);
+            if (row_written) row_written[r] = 1;
+        }
+    }
+    return status;
+}
+
+/*
+ * Step 2 (up-projection), the triple loop: for every written row r and output column n,
+ * k[r, n] = bf16_rne( sum_{k < R} latent[r, k] * W[n, k] ), summed in fp64 in order of k.
+ * W is [n_out, R] with R contiguous (weight "[num_heads * qk_nope_head_dim,
+ * kv_latent_dim]"); only the first R columns of a latent row are multiplied.
+ */
+void oracle_up_project_bf16(const uint16_t* k_latent, int32_t latent_cols,
+                            const uint8_t* row_written, int32_t buffer_length,
+                            const uint16_t* w, int32_t kv_lora_rank, int32_t n_out,
+                            uint16_t* k_buffer) {
+    for (int64_t r = 0; r < buffer_length; ++r) {
+        if (row_written && !row_written[r]) continue;
+        const uint16_t* a = k_latent + r * latent_cols;
+        for (int64_t n = 0; n < n_out; ++n) {
+            const uint16_t* wn = w + n * kv_lora_rank;
+            double acc = 0.0;
+            for (int64_t k = 0; k < kv_lora_rank; ++k)
+                acc += oracle_bf16_to_double(a[k]) * oracle_bf16_to_double(wn[k]);
+            k_buffer[r * n_out + n] = oracle_double_to_bf16(acc);
+        }
+    }
+}
+
+/* Whole bf16 decompress = step 1 then step 2.  Returns step 1's status. */
+int oracle_decompress_k(const uint16_t* cache, int64_t layer_stride, int64_t page_stride,
+                        int64_t slot_stride, int32_t num_pages, int32_t page_size,
+                        const uint32_t* page_table, int32_t max_pages_per_seq,
+                        uint32_t layer_idx, const uint32_t* buffer_row_offsets,
+                        const uint32_t* cache_offsets, int32_t batch, int32_t buffer_length,
+                        int32_t kv_lora_rank, int32_t rope_dim, const uint16_t* w,
+                        int32_t n_out, uint16_t* k_latent, uint16_t* k_buffer,
+                        uint8_t* row_written) {
+    int32_t latent_cols = kv_lora_rank + rope_dim;
+    int st = oracle_gather_latent(cache, layer_stride, page_stride, slot_stride, num_pages,
+                                  page_size, page_table, max_pages_per_seq, layer_idx,
+                                  buffer_row_offsets, cache_offsets, batch, buffer_length,
+                                  latent_cols, k_latent, row_written);
+    oracle_up_project_bf16(k_latent, latent_cols, row_written, buffer_length, w,
+                           kv_lora_rank, n_out, k_buffer);
+    return st;
+}
+
+/*
+ * Single-row form for sampled checks at full size: computes row `r` alone by finding the
+ * request whose range [bro[b], bro[b+1]) holds r (a linear scan), then the same copy and
+ * dot products.  Returns 0 when the row is written, 1 when no request covers it or
+ * r >= buffer_length, 4 when its token resolves outside the page table / cache.
+ */
+int oracle_decompress_k_row(const uint16_t* cache, int64_t layer_stride,
+                            int64_t page_stride, int64_t slot_stride, int32_t num_pages,
+                            int32_t page_size, const uint32_t* page_table,
+                            int32_t max_pages_per_seq, uint32_t layer_idx,
+                            const uint32_t* buffer_row_offsets,
+                            const uint32_t* cache_offsets, int32_t batch,
+                            int32_t buffer_length, int32_t kv_lora_rank, int32_t rope_dim,
+                            const uint16_t* w, int32_t n_out, int64_t r,
+                            uint16_t* latent_row, uint16_t* k_row) {
+    if (r < 0 || r >= buffer_length) return 1;
+    int32_t latent_cols = kv_lora_rank + rope_dim;
+    for (int32_t b = 0; b < batch; ++b) {
+        if ((uint64_t)buffer_row_offsets[b] <= (uint64_t)r &&
+            (uint64_t)r < (uint64_t)buffer_row_offsets[b + 1]) {
+            uint64_t t = (uint64_t)cache_offsets[b] + ((uint64_t)r - buffer_row_offsets[b]);
+            int64_t off = token_offset(page_table, max_pages_per_seq, num_pages, page_size,
+                                       page_stride, slot_stride, b, t);
+            if (off < 0) return 4;
+            const uint16_t* src = cache + (int64_t)layer_idx * layer_stride + off;
+            memcpy(latent_row, src, sizeof(uint16_t) * (size_t)latent_cols);
+            for (int64_t n = 0; n < n_out; ++n) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < kv_lora_rank; ++k)
+                    acc += oracle_bf16_to_double(latent_row[k]) *
+                           oracle_bf16_to_double(w[n * kv_lora_rank + k]);
+                k_row[n] = oracle_double_to_bf16(acc);
+            }
+            return 0;
+        }
+    }
+    return 1;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* FP8 block-scaled decompress (the decompress stage of mla_prefill_decode_graph_fp8)     */
+/* ------------------------------------------------------------------------------------ */
+
+/*
+ * Activation quantisation of one latent row, 1 x 128 blocks over the first R columns
+ * (m_scale_granularity = 1, k_scale_granularity = 128).  Reading of the silent points:
+ * the block scale is s = amax / 448 in fp32 (448 = largest finite e4m3), or 1 when the
+ * block is all zeros; each element is q = e4m3_rne_satfinite(x / s) with the division
+ * in fp32, correctly rounded.  Writes R codes and R/128 scales.
+ */
+void oracle_quantize_row_e4m3(const uint16_t* latent_row, int32_t kv_lora_rank,
+                              uint8_t* q_row, float* scale_row) {
+    for (int32_t kb = 0; kb < kv_lora_rank / 128; ++kb) {
+        float amax = 0.0f;
+        for (int32_t k = kb * 128; k < kb * 128 + 128; ++k) {
+            float v = fabsf((float)oracle_bf16_to_double(latent_row[k]));
+            if (v > amax) amax = v;
+        }
+        float s = (amax > 0.0f) ? amax / 448.0f : 1.0f;
+        scale_row[kb] = s;
+        for (int32_t k = kb * 128; k < kb * 128 + 128; ++k) {
+            float x = (float)oracle_bf16_to_double(latent_row[k]);
+            float y = x / s;
+            q_row[k] = oracle_float_to_e4m3_satfinite(y);
+        }
+    }
+}
+
+/*
+ * Block-scaled product of one quantised row with the e4m3 weight:
+ *   k[n] = bf16_rne( sum_kb  sa[kb] * sw[n/128, kb] * sum_{k in kb} dq(q[k]) * dq(qw[n, k]) )
+ * in fp64 on the dequantised values.  qw is [n_out, R] (R contiguous); sw is
+ * [n_out/128, R/128] (n_scale_granularity = k_scale_granularity = 128).
+ */
+static void fp8_row_product(const uint8_t* q_row, const float* sa_row, const uint8_t* qw,
+                            const float* sw, int32_t kv_lora_rank, int32_t n_out,
+                            uint16_t* k_row) {
+    int32_t kblocks = kv_lora_rank / 128;
+    for (int64_t n = 0; n < n_out; ++n) {
+        double total = 0.0;
+        for (int32_t kb = 0; kb < kblocks; ++kb) {
+            double part = 0.0;
+            for (int64_t k = (int64_t)kb * 128; k < (int64_t)kb * 128 + 128; ++k)
+                part += oracle_e4m3_to_double(q_row[k]) *
+                        oracle_e4m3_to_double(qw[n * kv_lora_rank + k]);
+            total += (double)sa_row[kb] * (double)sw[(n / 128) * kblocks + kb] * part;
+        }
+        k_row[n] = oracle_double_to_bf16(total);
+    }
+}
+
+/*
+ * Whole FP8 decompress: gather (bit copy, as in the bf16 path; k_latent keeps all C bf16
+ * columns, rope included), quantise every written row, then the block-scaled product.
+ * q_latent [buffer_length, R] and q_scale [buffer_length, R/128] receive the quantised
+ * activations of the written rows.  Returns the gather's status.
+ */
+int oracle_decompress_k_fp8(const uint16_t* cache, int64_t layer_stride, int64_t page_stride,
+                            int64_t slot_stride, int32_t num_pages, int32_t page_size,
+                            const uint32_t* page_table, int32_t max_pages_per_seq,
+                            uint32_t layer_idx, const uint32_t* buffer_row_offsets,
+                            const uint32_t* cache_offsets, int32_t batch,
+                            int32_t buffer_length, int32_t kv_lora_rank, int32_t rope_dim,
+                            const uint8_t* w_e4m3, const float* w_scale, int32_t n_out,
+                            uint16_t* k_latent, uint16_t* k_buffer, uint8_t* q_latent,
+                            float* q_scale, uint8_t* row_written) {
+    int32_t latent_cols = kv_lora_rank + rope_dim;
+    int st = oracle_gather_latent(cache, layer_stride, page_stride, slot_stride, num_pages,
+                                  page_size, page_table, max_pages_per_seq, layer_idx,
+                                  buffer_row_offsets, cache_offsets, batch, buffer_length,
+                                  latent_cols, k_latent, row_written);
+    int32_t kblocks = kv_lora_rank / 128;
+    for (int64_t r = 0; r < buffer_length; ++r) {
+        if (!row_written[r]) continue;
+        oracle_quantize_row_e4m3(k_latent + r * latent_cols, kv_lora_rank,
+                                 q_latent + r * kv_lora_rank, q_scale + r * kblocks);
+        fp8_row_product(q_latent + r * kv_lora_rank, q_scale + r * kblocks, w_e4m3, w_scale,
+                        kv_lora_rank, n_out, k_buffer + r * n_out);
+    }
+    return st;
+}
+
+/* Single-row FP8 form (same return codes as oracle_decompress_k_row). */
+int oracle_decompress_k_fp8_row(const uint16_t* cache, int64_t layer_stride,
+                                int64_t page_stride, int64_t slot_stride, int32_t num_pages,
+                                int32_t page_size, const uint32_t* page_table,
+                                int32_t max_pages_per_seq, uint32_t layer_idx,
+                                const uint32_t* buffer_row_offsets,
+                                const uint32_t* cache_offsets, int32_t batch,
+                                int32_t buffer_length, int32_t kv_lora_rank,
+                                int32_t rope_dim, const uint8_t* w_e4m3,
+                                const float* w_scale, int32_t n_out, int64_t r,
+                                uint16_t* latent_row, uint16_t* k_row, uint8_t* q_row,
+                                float* scale_row) {
+    if (r < 0 || r >= buffer_length) return 1;
+    int32_t latent_cols = kv_lora_rank + rope_dim;
+    for (int32_t b = 0; b < batch; ++b) {
+        if ((uint64_t)buffer_row_offsets[b] <= (uint64_t)r &&
+            (uint64_t)r < (uint64_t)buffer_row_offsets[b + 1]) {
+            uint64_t t = (uint64_t)cache_offsets[b] + ((uint64_t)r - buffer_row_offsets[b]);
+            int64_t off = token_offset(page_table, max_pages_per_seq, num_pages, page_size,
+                                       page_stride, slot_stride, b, t);
+            if (off < 0) return 4;
+            memcpy(latent_row, cache + (int64_t)layer_idx * layer_stride + off,
+                   sizeof(uint16_t) * (size_t)latent_cols);
+            oracle_quantize_row_e4m3(latent_row, kv_lora_rank, q_row, scale_row);
+            fp8_row_product(q_row, scale_row, w_e4m3, w_scale, kv_lora_rank, n_out, k_row);
+            return 0;
+        }
+    }
+    return 1;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* kv_matmul_ragged_paged                                                                */
+/* ------------------------------------------------------------------------------------ */
+
+/*
+ * Y = hidden_state x weight, hidden_state [total_rows, k_in] (k_in contiguous), weight
+ * [k_in, n_out] (n_out contiguous), summed in fp64 in order of k, rounded to bf16.
+ * Row r of request b (i = r - iro[b]) lands at cache position pos = cache_lengths[b] + i:
+ * page = page_table[b][pos / page_size], slot = pos % page_size.  Columns
+ * [0, head_elems) go to the K plane of `layer`, columns [head_elems, 2*head_elems) to the
+ * V plane (kv_stride elements further); n_out is head_elems (K only) or 2*head_elems.
+ * Nothing else in the cache is written.  Returns 0, or 4 if some row resolved outside the
+ * page table / cache (that row is skipped).
+ */
+int oracle_kv_matmul(const uint16_t* hidden_state, const uint32_t* input_row_offsets,
+                     int32_t batch, int32_t total_rows, int32_t k_in, const uint16_t* weight,
+                     int32_t n_out, uint16_t* cache, int64_t layer_stride,
+                     int64_t page_stride, int64_t slot_stride, int64_t kv_stride,
+                     int32_t num_pages, int32_t page_size, int32_t head_elems,
+                     const uint32_t* page_table, int32_t max_pages_per_seq,
+                     const uint32_t* cache_lengths, uint32_t layer_idx) {
+    int status = 0;
+    uint16_t* layer = cache + (int64_t)layer_idx * layer_stride;
+    for (int32_t b = 0; b < batch; ++b) {
+        uint32_t begin = input_row_offsets[b];
+        uint32_t end = input_row_offsets[b + 1];
+        for (uint32_t i = 0; begin + i < end; ++i) {
+            uint64_t r = (uint64_t)begin + i;
+            if (r >= (uint64_t)total_rows) break;
+            uint64_t pos = (uint64_t)cache_lengths[b] + i;
+            int64_t off = token_offset(page_table, max_pages_per_seq, num_pages, page_size,
+                                       page_stride, slot_stride, b, pos);
+            if (off < 0) {
+                status = 4;
+                continue;
+            }
+            for (int64_t n = 0; n < n_out; ++n) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < k_in; ++k)
+                    acc += oracle_bf16_to_double(hidden_state[r * k_in + k]) *
+                           oracle_bf16_to_double(weight[k * n_out + n]);
+                int64_t plane = (n < head_elems) ? 0 : kv_stride;
+                layer[plane + off + (n % head_elems)] = oracle_double_to_bf16(acc);
+            }
+        }
+    }
+    return status;
+}

@@ -1,0 +1,317 @@
+"""Seeded synthetic inputs for the paged-KV MLA hot path.
+
+This module only draws random numbers and lays them out; it holds none of the method's
+arithmetic (no gather, no product, no rounding of results).  Both the CUDA path's tests /
+benchmark and the CPU oracle consume the arrays it returns, so the two sides always see
+the same bytes.
+
+bf16 tensors are returned as uint16 bit patterns, e4m3 tensors as uint8 codes, metadata
+as uint32, scales as float32.  All generation uses a torch CPU ``Generator`` seeded per
+workload, so every array is reproducible on any host.
+
+Workload shapes (the MLA decompress of DeepSeek-V3-shaped latent caches and the
+kv_matmul write path):
+  * tiny decompress: 2 requests (5 and 11 cached tokens), page_size 4, 8 pages assigned by a
+    seeded permutation, kv_lora_rank 64 + rope 16, W_k [64, 64].
+  * DeepSeek-V3-shaped decompress: 16 requests, lengths ~U[512, 4096], cache_offsets
+    ~U[0, len/4] with the copied range running to the end of the history, page_size 128,
+    shuffled pages, kv_lora_rank 512 + rope 64, W_k [16384, 512] ~N(0, 1/sqrt(512)).
+  * the same shapes with an e4m3 W_k and fp32 scales per 128x128 block.
+  * long-context decompress: 4 requests x 32768 tokens, 1024 shuffled pages.
+  * kv_matmul: 32 requests, new tokens ~U[1, 512], cache lengths ~U[0, 2048],
+    hidden_state [sum(new), 4096] ~N(0,1), weight [4096, 2048] ~N(0, 1/64), K/V planes of
+    8 kv heads x 128, page_size 128, cache pre-filled with sentinels.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional
+
+import numpy as np
+import torch
+
+PAGE_TABLE_PAD = 0xFFFFFFFF  # unused page-table entries (never read by a correct walk)
+SENTINEL_K = 0x7FA1          # bf16 NaN patterns no finite product can produce
+SENTINEL_V = 0x7FA2
+SENTINEL_OUT = 0x7FA3
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator()
+    g.manual_seed(int(seed))
+    return g
+
+
+def bf16_normal(shape, std: float, g: torch.Generator) -> np.ndarray:
+    """N(0, std^2) samples rounded to bf16 by torch, returned as uint16 bit patterns."""
+    t = torch.randn(*shape, generator=g, dtype=torch.float32) * float(std)
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_small_ints(shape, lo: int, hi: int, g: torch.Generator) -> np.ndarray:
+    """Integers in [lo, hi] stored as bf16 bit patterns (exact)."""
+    t = torch.randint(lo, hi + 1, shape, generator=g).to(torch.float32)
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_bits_to_float(a: np.ndarray) -> np.ndarray:
+    """Widen uint16 bf16 patterns to float32 (a bit shift; exact)."""
+    return (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def quantize_weight_e4m3(w: torch.Tensor, block: int = 128):
+    """Input preparation for the FP8 workloads: per 128x128 block of an fp32 weight,
+    scale = amax / 448 (1 for an all-zero block) and codes = torch's float8_e4m3fn cast of
+    w / scale.  The kernel under test receives these codes and scales as given."""
+    n, k = w.shape
+    wb = w.reshape(n // block, block, k // block, block)
+    amax = wb.abs().amax(dim=(1, 3))
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    q = (wb / scale[:, None, :, None]).reshape(n, k).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).numpy().copy(), scale.to(torch.float32).numpy().copy()
+
+
+@dataclass
+class DecompressInputs:
+    """One decompress problem.  cache is [num_layers, num_pages, page_size, slot_elems]."""
+    name: str
+    cache: np.ndarray
+    page_table: np.ndarray          # uint32 [batch, max_pages_per_seq]
+    buffer_row_offsets: np.ndarray  # uint32 [batch + 1]
+    cache_offsets: np.ndarray       # uint32 [batch + 1] (last entry unused)
+    buffer_length: int
+    kv_lora_rank: int
+    rope_dim: int
+    n_out: int
+    layer_idx: int
+    w_k: Optional[np.ndarray] = None        # uint16 bf16 [n_out, kv_lora_rank]
+    w_k_e4m3: Optional[np.ndarray] = None   # uint8 [n_out, kv_lora_rank]
+    w_k_scale: Optional[np.ndarray] = None  # float32 [n_out/128, kv_lora_rank/128]
+    lengths: Optional[np.ndarray] = None
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def batch(self) -> int:
+        return int(self.page_table.shape[0])
+
+    @property
+    def latent_cols(self) -> int:
+        return self.kv_lora_rank + self.rope_dim
+
+    @property
+    def num_layers(self) -> int:
+        return int(self.cache.shape[0])
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.cache.shape[1])
+
+    @property
+    def page_size(self) -> int:
+        return int(self.cache.shape[2])
+
+    @property
+    def slot_elems(self) -> int:
+        return int(self.cache.shape[3])
+
+    @property
+    def strides(self):
+        """(layer_stride, page_stride, slot_stride) in elements."""
+        _, P, S, E = self.cache.shape
+        return P * S * E, S * E, E
+
+    @property
+    def flops(self) -> int:
+        rows = min(int(self.buffer_row_offsets[-1]), self.buffer_length)
+        return 2 * rows * self.kv_lora_rank * self.n_out
+
+
+def _assign_pages(pages_needed, total_pages, g):
+    perm = torch.randperm(total_pages, generator=g).numpy().astype(np.uint32)
+    maxp = max(1, max(pages_needed) if len(pages_needed) else 1)
+    pt = np.full((len(pages_needed), maxp), PAGE_TABLE_PAD, np.uint32)
+    nxt = 0
+    for b, n in enumerate(pages_needed):
+        pt[b, :n] = perm[nxt:nxt + n]
+        nxt += n
+    return pt
+
+
+def make_decompress(name, seed, lengths, cache_offsets, page_size, kv_lora_rank, rope_dim, n_out,
+                    num_layers=1, layer_idx=0, extra_pages=0, w_std=None, fp8=False,
+                    int_values=False, slot_pad=0, page_table=None, num_pages=None,
+                    buffer_length=None) -> DecompressInputs:
+    """General seeded decompress problem.  Request b copies cache tokens
+    [cache_offsets[b], lengths[b]) into rows [bro[b], bro[b+1]) of the ragged buffer."""
+    g = _gen(seed)
+    lengths = np.asarray(lengths, np.int64)
+    co = np.asarray(cache_offsets, np.int64)
+    B = len(lengths)
+    rows = lengths - co
+    assert (rows >= 0).all()
+    bro = np.zeros(B + 1, np.uint32)
+    bro[1:] = np.cumsum(rows)
+    C = kv_lora_rank + rope_dim
+    pages_needed = [int(math.ceil(l / page_size)) for l in lengths]
+    if page_table is None:
+        total_pages = sum(pages_needed) + extra_pages
+        pt = _assign_pages(pages_needed, total_pages, g)
+    else:
+        pt = np.asarray(page_table, np.uint32)
+        total_pages = int(num_pages)
+    slot_elems = C + slot_pad
+    shape = (num_layers, total_pages, page_size, slot_elems)
+    if int_values:
+        cache = bf16_small_ints(shape, -8, 8, g)
+    else:
+        cache = bf16_normal(shape, 1.0, g)
+    L = int(bro[-1]) if buffer_length is None else int(buffer_length)
+    d = DecompressInputs(name=name, cache=cache, page_table=pt, buffer_row_offsets=bro,
+                         cache_offsets=np.concatenate([co, [0]]).astype(np.uint32), buffer_length=L,
+                         kv_lora_rank=kv_lora_rank, rope_dim=rope_dim, n_out=n_out,
+                         layer_idx=layer_idx, lengths=lengths)
+    std = w_std if w_std is not None else 1.0 / math.sqrt(kv_lora_rank)
+    if fp8:
+        w = torch.randn(n_out, kv_lora_rank, generator=g, dtype=torch.float32) * std
+        d.w_k_e4m3, d.w_k_scale = quantize_weight_e4m3(w)
+    elif int_values:
+        d.w_k = bf16_small_ints((n_out, kv_lora_rank), -2, 2, g)
+    else:
+        d.w_k = bf16_normal((n_out, kv_lora_rank), std, g)
+    return d
+
+
+def tiny_decompress(seed=1000) -> DecompressInputs:
+    """2 requests of 5 and 11 cached tokens, cache_offsets 0, page_size 4, 8 pages given by a
+    seeded permutation reshaped to the [2, 4] page table, latent 64 + 16, W_k [64, 64]."""
+    g = _gen(seed)
+    pt = torch.randperm(8, generator=g).numpy().astype(np.uint32).reshape(2, 4)
+    return make_decompress("tiny_decompress", seed + 1, [5, 11], [0, 0], 4, 64, 16, 64,
+                           w_std=1.0 / math.sqrt(64), page_table=pt, num_pages=8)
+
+
+def deepseek_lengths(seed, batch=16, lo=512, hi=4096):
+    g = _gen(seed)
+    lengths = torch.randint(lo, hi + 1, (batch,), generator=g).numpy().astype(np.int64)
+    co = np.array([int(torch.randint(0, l // 4 + 1, (1,), generator=g)) for l in lengths], np.int64)
+    return lengths, co
+
+
+def deepseek_decompress(seed=1001, fp8=False) -> DecompressInputs:
+    """16 requests, len ~U[512,4096], cache_offsets ~U[0,len/4], page_size 128, shuffled
+    pages, latent 512 + 64, W_k [16384, 512]."""
+    lengths, co = deepseek_lengths(seed)
+    return make_decompress("deepseek_v3_fp8_decompress" if fp8 else "deepseek_v3_bf16_decompress",
+                           seed + 1, lengths, co, 128, 512, 64, 16384, fp8=fp8)
+
+
+def long_context_decompress(seed=1003) -> DecompressInputs:
+    """4 requests x 32768 cached tokens (buffer_length 131072), 1024 shuffled pages."""
+    return make_decompress("long_context_decompress", seed, [32768] * 4, [0] * 4, 128, 512, 64,
+                           16384)
+
+
+@dataclass
+class KvMatmulInputs:
+    """One kv_matmul problem.  cache is [num_layers, 2 (K, V), num_pages, page_size,
+    head_elems]; hidden_state [total_rows, k_in]; weight [k_in, n_out] (n_out contiguous)."""
+    name: str
+    hidden_state: np.ndarray
+    input_row_offsets: np.ndarray
+    weight: np.ndarray
+    cache: np.ndarray
+    page_table: np.ndarray
+    cache_lengths: np.ndarray
+    head_elems: int
+    layer_idx: int
+    new_tokens: Optional[np.ndarray] = None
+
+    @property
+    def batch(self) -> int:
+        return int(self.cache_lengths.shape[0])
+
+    @property
+    def total_rows(self) -> int:
+        return int(self.hidden_state.shape[0])
+
+    @property
+    def k_in(self) -> int:
+        return int(self.weight.shape[0])
+
+    @property
+    def n_out(self) -> int:
+        return int(self.weight.shape[1])
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.cache.shape[2])
+
+    @property
+    def page_size(self) -> int:
+        return int(self.cache.shape[3])
+
+    @property
+    def strides(self):
+        """(layer_stride, page_stride, slot_stride, kv_stride) in elements."""
+        _, two, P, S, E = self.cache.shape
+        return two * P * S * E, S * E, E, P * S * E
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.total_rows * self.k_in * self.n_out
+
+    @property
+    def bytes_moved(self) -> int:
+        """Algorithmic HBM bytes: read hidden_state and weight once, write every output."""
+        return 2 * (self.total_rows * self.k_in + self.k_in * self.n_out +
+                    self.total_rows * self.n_out)
+
+
+def make_kv_matmul(name, seed, new_tokens, cache_lengths, k_in, num_kv_heads, head_dim,
+                   page_size, num_layers=1, layer_idx=0, k_only=False, extra_pages=0,
+                   int_values=False, w_std=None) -> KvMatmulInputs:
+    g = _gen(seed)
+    new_tokens = np.asarray(new_tokens, np.int64)
+    cache_lengths = np.asarray(cache_lengths, np.int64)
+    B = len(new_tokens)
+    iro = np.zeros(B + 1, np.uint32)
+    iro[1:] = np.cumsum(new_tokens)
+    M = int(iro[-1])
+    HD = num_kv_heads * head_dim
+    n_out = HD if k_only else 2 * HD
+    pages_needed = [int(math.ceil((c + n) / page_size)) for c, n in zip(cache_lengths, new_tokens)]
+    total_pages = sum(pages_needed) + extra_pages
+    pt = _assign_pages(pages_needed, total_pages, g)
+    if int_values:
+        hidden = bf16_small_ints((M, k_in), -4, 4, g)
+        weight = bf16_small_ints((k_in, n_out), -2, 2, g)
+    else:
+        hidden = bf16_normal((M, k_in), 1.0, g)
+        weight = bf16_normal((k_in, n_out), w_std if w_std is not None else 1.0 / math.sqrt(k_in), g)
+    cache = np.empty((num_layers, 2, total_pages, page_size, HD), np.uint16)
+    cache[:, 0] = SENTINEL_K
+    cache[:, 1] = SENTINEL_V
+    return KvMatmulInputs(name=name, hidden_state=hidden, input_row_offsets=iro, weight=weight,
+                          cache=cache, page_table=pt, cache_lengths=cache_lengths.astype(np.uint32),
+                          head_elems=HD, layer_idx=layer_idx, new_tokens=new_tokens)
+
+
+def kv_matmul_write_path(seed=1004) -> KvMatmulInputs:
+    """32 requests, new ~U[1,512], cache_len ~U[0,2048], hidden [sum(new), 4096] ~N(0,1),
+    weight [4096, 2048] ~N(0, 1/64), 8 kv heads x 128 (K then V), page_size 128."""
+    g = _gen(seed)
+    new = torch.randint(1, 513, (32,), generator=g).numpy()
+    cl = torch.randint(0, 2049, (32,), generator=g).numpy()
+    return make_kv_matmul("kv_matmul_write_path", seed + 1, new, cl, 4096, 8, 128, 128,
+                          w_std=1.0 / 64)
+
+
+# Names used by tests and the benchmark.
+WORKLOADS = {
+    "tiny_decompress": tiny_decompress,
+    "deepseek_v3_bf16_decompress": lambda: deepseek_decompress(1001, fp8=False),
+    "deepseek_v3_fp8_decompress": lambda: deepseek_decompress(1001, fp8=True),
+    "long_context_decompress": long_context_decompress,
+    "kv_matmul_write_path": kv_matmul_write_path,
+}
