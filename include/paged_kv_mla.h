@@ -1,0 +1,211 @@
+/*
+ * paged_kv_mla.h -- C ABI of the GB300 (sm_103a) paged-KV MLA hot path.
+ *
+ * Three operations, after the Modular MAX kernel pages that define them:
+ *
+ *   mla_decompress_k_paged      generic_flare_mla_decompress_k_cache_ragged_paged
+ *                               (nn/kv_cache_ragged; signature, description and Args):
+ *                               gather each request's latent K rows out of a paged cache
+ *                               into k_latent_buffer, then k_buffer = latent[:, :R] . W_k^T.
+ *   mla_decompress_k_paged_fp8  the same decompress as the K-decompress stage of
+ *                               mla_prefill_decode_graph_fp8 (attention/gpu/mla_graph;
+ *                               Parameters m/n/k_scale_granularity, Args w_k, w_k_scale,
+ *                               buffer_row_offsets, cache_offsets, buffer_length), with an
+ *                               e4m3 W_k carrying 128x128 fp32 block scales and the latent
+ *                               quantised per token per 128-column block.
+ *   kv_matmul_paged             kv_matmul_ragged_paged (nn/kv_cache_ragged; description and
+ *                               Args): Y = hidden_state . weight on the ragged rows, with
+ *                               row i of request b written into the paged K/V cache at
+ *                               position cache_lengths[b] + i.
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor argument is DEVICE memory on the current CUDA device, allocated and
+ *     owned by the caller.  Shape scalars are host values.  The library keeps no pointer
+ *     after a call returns and allocates no device memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous on it; outputs are valid once the stream has reached the call.
+ *   - The return value reports what the host can check before launching: a NULL
+ *     required pointer, misaligned pointer or stride (16-byte rules below), a size the
+ *     kernels do not support, or a failed CUDA launch.  Nothing is launched when it is
+ *     not PKM_OK.  A call with nothing to do (no rows or no requests) returns PKM_OK
+ *     after checking only its sizes, and launches nothing.
+ *   - `dev_status` (nullable, device int32) receives errors found on the device, merged
+ *     with atomicMax: PKM_ERR_OUT_OF_RANGE when a token resolves past the page table row
+ *     or to a page id >= num_pages (that row is then neither read nor written), and
+ *     PKM_ERR_TIMEOUT when an internal pipeline wait exceeded its limit (about one
+ *     second, PKM_WAIT_TIMEOUT_MS overrides) and the kernel stopped early.  The caller
+ *     zeroes it and reads it after synchronising.
+ *   - The kernels never trap and never write outside the rows / cache slots the
+ *     operation defines.
+ *   - bf16 values are IEEE binary32 truncated to 16 bits; products accumulate in fp32 on
+ *     the tensor cores and are rounded to bf16 with round-to-nearest-even.
+ */
+#ifndef PAGED_KV_MLA_H
+#define PAGED_KV_MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKM_OK = 0,
+    PKM_ERR_INVALID_ARG = 1,   /* NULL / misaligned pointer, negative or inconsistent size */
+    PKM_ERR_UNSUPPORTED = 2,   /* a size outside what the kernels implement */
+    PKM_ERR_CUDA = 3,          /* a CUDA runtime / driver call failed */
+    PKM_ERR_OUT_OF_RANGE = 4,  /* device: a token resolved outside the page table / cache */
+    PKM_ERR_TIMEOUT = 5        /* device: a pipeline wait timed out, the kernel stopped */
+} pkm_status;
+
+/*
+ * One paged cache (the PagedKVCacheCollection of the pages, for all layers), described by
+ * element strides so that any row-contiguous layout can be addressed.  The slot of token t
+ * of request b in layer l is
+ *     data + l*layer_stride + page_table[b*max_pages_per_seq + t/page_size]*page_stride
+ *          + (t % page_size)*slot_stride            (+ kv_stride for the V plane)
+ * and holds row_elems contiguous bf16 values.
+ *   data              device, bf16, 16-byte aligned.
+ *   *_stride          in elements; layer/page/slot/kv strides must be multiples of 8
+ *                     (16 bytes).
+ *   num_layers        layers in `data`; layer_idx must be below it.
+ *   num_pages         physical pages per layer; page ids >= num_pages are out of range.
+ *   page_size         tokens per page (> 0).
+ *   row_elems         values per slot that the operation reads or writes: the latent width
+ *                     kv_lora_rank + qk_rope_head_dim for the decompress entry points,
+ *                     num_kv_heads*head_size for kv_matmul_paged (per plane).
+ *   page_table        device uint32 [batch, max_pages_per_seq], row-major.
+ *   cache_lengths     device uint32 [batch]: tokens already in the cache per request.  Read
+ *                     by kv_matmul_paged only (and never updated by it); may be NULL for
+ *                     the decompress entry points.
+ *   kv_stride         offset of the V plane from the K plane; kv_matmul_paged only.
+ */
+typedef struct {
+    void* data;
+    int64_t layer_stride;
+    int64_t page_stride;
+    int64_t slot_stride;
+    int64_t kv_stride;
+    int32_t num_layers;
+    int32_t num_pages;
+    int32_t page_size;
+    int32_t row_elems;
+    const uint32_t* page_table;
+    int32_t max_pages_per_seq;
+    const uint32_t* cache_lengths;
+} pkm_paged_cache;
+
+/*
+ * bf16 latent-K decompress.
+ * Source: generic_flare_mla_decompress_k_cache_ragged_paged -- signature, description
+ * ("gathers ... into k_latent_buffer using buffer_row_offsets and cache_offsets, then
+ * multiplies by the ... weight"), Args buffer_row_offsets_1d, cache_offsets_1d,
+ * buffer_length, weight, kv_collection, layer_idx, k_latent_buffer, k_buffer.
+ *
+ * For every request b < batch and i < buffer_row_offsets[b+1] - buffer_row_offsets[b]:
+ *     r = buffer_row_offsets[b] + i          (skipped when r >= buffer_length)
+ *     t = cache_offsets[b] + i               (cache token, resolved through the page table)
+ *     k_latent_buffer[r, 0:C] = cache slot of t, bit for bit, C = kv_lora_rank + rope_dim
+ *     k_buffer[r, n] = bf16( sum_{k < kv_lora_rank} k_latent_buffer[r, k] * w_k[n, k] )
+ * Rows of the outputs that no request covers (r >= buffer_row_offsets[batch], or
+ * r < buffer_row_offsets[0]) are left untouched.
+ *
+ *   cache                host struct; cache->row_elems must equal C.
+ *   buffer_row_offsets   device uint32 [batch+1], non-decreasing.
+ *   cache_offsets        device uint32 [>= batch]; entries past batch-1 are not read.
+ *   buffer_length        rows of k_latent_buffer and k_buffer (>= 0; 0 launches nothing).
+ *   kv_lora_rank         R: multiple of 64, 64..512.
+ *   rope_dim             P: C = R + P must be a multiple of 8.
+ *   w_k                  device bf16 [n_out, R], R contiguous, 16-byte aligned.
+ *   n_out                num_heads * qk_nope_head_dim: a multiple of 64.
+ *   k_latent_buffer      device bf16 [buffer_length, C], row-major, 16-byte aligned.
+ *   k_buffer             device bf16 [buffer_length, n_out], row-major, 16-byte aligned.
+ */
+pkm_status mla_decompress_k_paged(const pkm_paged_cache* cache, uint32_t layer_idx,
+                                  const uint32_t* buffer_row_offsets,
+                                  const uint32_t* cache_offsets, int32_t batch,
+                                  int32_t buffer_length, int32_t kv_lora_rank,
+                                  int32_t rope_dim, const void* w_k, int32_t n_out,
+                                  void* k_latent_buffer, void* k_buffer, int32_t* dev_status,
+                                  void* stream);
+
+/*
+ * Bytes of device workspace mla_decompress_k_paged_fp8 needs for buffer_length rows of
+ * kv_lora_rank latent columns (0 for invalid sizes).  Layout, for a caller that wants to
+ * read the quantised activations back:
+ *     offset 0                                 e4m3 codes [buffer_length, kv_lora_rank]
+ *     offset align256(buffer_length*R)         fp32 scales [buffer_length, kv_lora_rank/128]
+ */
+size_t mla_decompress_k_paged_fp8_workspace_size(int32_t buffer_length, int32_t kv_lora_rank);
+
+/*
+ * FP8 block-scaled latent-K decompress.
+ * Source: mla_prefill_decode_graph_fp8 -- Parameters fp8_dtype, fp8_scale_dtype,
+ * m_scale_granularity, n_scale_granularity, k_scale_granularity; Args buffer_row_offsets,
+ * cache_offsets, buffer_length, w_k ("up-projecting the latent cache to full K",
+ * [num_heads * qk_nope_head_dim, kv_latent_dim]) and w_k_scale.  Granularities are fixed
+ * at m = 1, n = 128, k = 128.
+ *
+ * Same rows and the same k_latent_buffer copy as mla_decompress_k_paged (bf16, all C
+ * columns).  Then, per written row r and per 128-column block kb of its first R columns:
+ *     s[r, kb] = amax_k |x[r, k]| / 448 in fp32 (1 when the block is all zeros)
+ *     q[r, k]  = e4m3_rne_satfinite(x[r, k] / s[r, kb]), the division in fp32
+ *     k_buffer[r, n] = bf16( sum_kb s[r, kb] * w_k_scale[n/128, kb]
+ *                              * sum_{k in kb} q[r, k] * w_k_e4m3[n, k] )
+ *
+ *   kv_lora_rank         R: multiple of 128, 128..512.
+ *   w_k_e4m3             device e4m3 [n_out, R], R contiguous, 16-byte aligned.
+ *   w_k_scale            device fp32 [n_out/128, R/128], row-major.
+ *   n_out                multiple of 128.
+ *   workspace            device, >= mla_decompress_k_paged_fp8_workspace_size(...) bytes,
+ *                        256-byte aligned; receives q and s (layout above).
+ *   workspace_bytes      its size.
+ *   other arguments      as for mla_decompress_k_paged.
+ */
+pkm_status mla_decompress_k_paged_fp8(const pkm_paged_cache* cache, uint32_t layer_idx,
+                                      const uint32_t* buffer_row_offsets,
+                                      const uint32_t* cache_offsets, int32_t batch,
+                                      int32_t buffer_length, int32_t kv_lora_rank,
+                                      int32_t rope_dim, const void* w_k_e4m3,
+                                      const float* w_k_scale, int32_t n_out,
+                                      void* k_latent_buffer, void* k_buffer, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status,
+                                      void* stream);
+
+/*
+ * Ragged GEMM written into the paged K/V cache.
+ * Source: kv_matmul_ragged_paged -- description ("performs a matmul, writing the output
+ * into" the KV cache collection) and Args hidden_state (sum(seq_lens), num_heads *
+ * head_size), input_row_offsets (batch_size + 1), weight (num_heads * head_size,
+ * num_kv_heads * head_size), kv_collection (keys and values), layer_idx.
+ *
+ * For every request b < batch and i < input_row_offsets[b+1] - input_row_offsets[b]:
+ *     r = input_row_offsets[b] + i              (skipped when r >= total_rows)
+ *     pos = cache->cache_lengths[b] + i          (resolved through the page table)
+ *     Y[r, :] = bf16( hidden_state[r, :] . weight )
+ *     K plane slot of pos (layer layer_idx)  <- Y[r, 0 : HD]
+ *     V plane slot of pos                    <- Y[r, HD : 2 HD]     (when n_out == 2 HD)
+ * with HD = cache->row_elems.  No other cache element is written.
+ *
+ *   hidden_state         device bf16 [total_rows, k_in], row-major, 16-byte aligned.
+ *   input_row_offsets    device uint32 [batch+1], non-decreasing.
+ *   total_rows           rows of hidden_state (>= 0; 0 launches nothing).
+ *   k_in                 num_heads * head_size: a multiple of 64.
+ *   weight               device bf16 [k_in, n_out], n_out contiguous, 16-byte aligned.
+ *   n_out                HD (K only) or 2*HD (K then V); HD a multiple of 64.
+ *   kv_cache             host struct; cache_lengths required, kv_stride used for V.
+ */
+pkm_status kv_matmul_paged(const void* hidden_state, const uint32_t* input_row_offsets,
+                           int32_t batch, int32_t total_rows, int32_t k_in,
+                           const void* weight, int32_t n_out, const pkm_paged_cache* kv_cache,
+                           uint32_t layer_idx, int32_t* dev_status, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* pkm_status_string(pkm_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_MLA_H */

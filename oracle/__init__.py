@@ -79,6 +79,10 @@ def lib():
                                            _i64, _i64, _i64, _i32, _i32, _i32, _u32p, _i32, _u32p,
                                            _u32]
             L.oracle_kv_matmul.restype = ctypes.c_int
+            _i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
+            L.oracle_kv_row_dest.argtypes = [_u32p, _i32, _i32, _u32p, _u32p, _i32, _i32, _i32, _i64,
+                                             _i64, _i64p]
+            L.oracle_kv_row_dest.restype = None
             _lib = L
     return _lib
 
@@ -249,3 +253,14 @@ def kv_matmul(hidden_state, input_row_offsets, batch, total_rows, weight, cache:
                                   cache.num_pages, cache.page_size, int(head_elems),
                                   cache.page_table, cache.max_pages_per_seq,
                                   _c(cache_lengths, np.uint32), int(layer_idx))
+
+
+def kv_row_dest(input_row_offsets, batch, total_rows, cache_lengths, cache: PagedCacheView):
+    """Addressing step of kv_matmul alone: per-row element offset of the receiving slot inside
+    the layer's K plane (-1 uncovered, -2 out of range)."""
+    dest = np.zeros(max(int(total_rows), 1), np.int64)
+    lib().oracle_kv_row_dest(_c(input_row_offsets, np.uint32), int(batch), int(total_rows),
+                             _c(cache_lengths, np.uint32), cache.page_table,
+                             cache.max_pages_per_seq, cache.num_pages, cache.page_size,
+                             cache.page_stride, cache.slot_stride, dest)
+    return dest[: int(total_rows)]

@@ -428,3 +428,28 @@ int oracle_kv_matmul(const uint16_t* hidden_state, const uint32_t* input_row_off
     }
     return status;
 }
+
+/*
+ * The addressing step of kv_matmul_ragged_paged alone, for checks at sizes where the
+ * oracle's GEMM is too slow: dest[r] (r < total_rows) = element offset, inside the K plane
+ * of the layer, of the slot that receives row r (same walk as oracle_kv_matmul), -1 when no
+ * request covers r, -2 when the position resolves outside the page table / cache.
+ */
+void oracle_kv_row_dest(const uint32_t* input_row_offsets, int32_t batch, int32_t total_rows,
+                        const uint32_t* cache_lengths, const uint32_t* page_table,
+                        int32_t max_pages_per_seq, int32_t num_pages, int32_t page_size,
+                        int64_t page_stride, int64_t slot_stride, int64_t* dest) {
+    for (int64_t r = 0; r < total_rows; ++r) dest[r] = -1;
+    for (int32_t b = 0; b < batch; ++b) {
+        uint32_t begin = input_row_offsets[b];
+        uint32_t end = input_row_offsets[b + 1];
+        for (uint32_t i = 0; begin + i < end; ++i) {
+            uint64_t r = (uint64_t)begin + i;
+            if (r >= (uint64_t)total_rows) break;
+            uint64_t pos = (uint64_t)cache_lengths[b] + i;
+            int64_t off = token_offset(page_table, max_pages_per_seq, num_pages, page_size,
+                                       page_stride, slot_stride, b, pos);
+            dest[r] = off < 0 ? -2 : off;
+        }
+    }
+}

@@ -1,0 +1,321 @@
+// api.cu -- the C entry points declared in include/paged_kv_mla.h: host-side argument
+// checks, tensor-map encoding, tile selection and kernel launches.  Every check that can
+// be made without touching the GPU is made before the first CUDA call, so invalid calls
+// return a status and launch nothing.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "paged_kv_mla.h"
+#include "pkm_internal.h"
+
+namespace {
+
+using pkm::DecompressArgs;
+using pkm::Fp8Extra;
+using pkm::KvMatmulArgs;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool mult8(int64_t v) { return v >= 0 && (v % 8) == 0; }
+
+uint64_t wait_timeout_ns() {
+    static uint64_t ns = [] {
+        const char* s = std::getenv("PKM_WAIT_TIMEOUT_MS");
+        long ms = s ? std::strtol(s, nullptr, 10) : 1000;
+        if (ms <= 0) ms = 1000;
+        return static_cast<uint64_t>(ms) * 1000000ull;
+    }();
+    return ns;
+}
+
+// Streaming multiprocessors of the current device (cached per device id).
+cudaError_t current_sm_count(int* out) {
+    static int counts[128] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    if (counts[dev] == 0) {
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        counts[dev] = n;
+    }
+    *out = counts[dev];
+    return cudaSuccess;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D row-major tensor [outer, inner] with a row pitch in bytes, boxes of
+// [box_outer, box_inner] elements, 128-byte swizzle, zero fill out of bounds.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_pitch_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+int pick_bn(int n_out) {
+    if (n_out % 256 == 0) return 256;
+    if (n_out % 128 == 0) return 128;
+    return 64;
+}
+
+// Checks shared by both decompress entry points.  Returns PKM_OK or the error.
+pkm_status check_decompress(const pkm_paged_cache* cache, uint32_t layer_idx, const uint32_t* bro,
+                            const uint32_t* co, int32_t batch, int32_t buffer_length,
+                            int32_t kv_lora_rank, int32_t rope_dim, const void* w, int32_t n_out,
+                            void* k_latent, void* k_buffer) {
+    if (cache == nullptr || bro == nullptr || co == nullptr || w == nullptr ||
+        k_latent == nullptr || k_buffer == nullptr || cache->data == nullptr ||
+        cache->page_table == nullptr)
+        return PKM_ERR_INVALID_ARG;
+    if (cache->num_layers <= 0 || layer_idx >= static_cast<uint32_t>(cache->num_layers) ||
+        cache->num_pages <= 0 || cache->page_size <= 0 || cache->max_pages_per_seq <= 0)
+        return PKM_ERR_INVALID_ARG;
+    if (cache->row_elems != kv_lora_rank + rope_dim) return PKM_ERR_INVALID_ARG;
+    if (!mult8(cache->layer_stride) || !mult8(cache->page_stride) || !mult8(cache->slot_stride))
+        return PKM_ERR_INVALID_ARG;
+    if (!aligned16(cache->data) || !aligned16(w) || !aligned16(k_latent) || !aligned16(k_buffer))
+        return PKM_ERR_INVALID_ARG;
+    if ((kv_lora_rank + rope_dim) % 8 != 0) return PKM_ERR_UNSUPPORTED;
+    return PKM_OK;
+}
+
+// Size checks that come before any pointer check: a call with nothing to do (no rows or no
+// requests) succeeds whatever its pointers are.
+pkm_status check_decompress_sizes(int32_t batch, int32_t buffer_length, int32_t kv_lora_rank,
+                                  int32_t rope_dim, int32_t n_out, bool* empty) {
+    if (batch < 0 || buffer_length < 0 || rope_dim < 0 || n_out <= 0 || kv_lora_rank <= 0)
+        return PKM_ERR_INVALID_ARG;
+    *empty = (buffer_length == 0 || batch == 0);
+    return PKM_OK;
+}
+
+DecompressArgs make_decompress_args(const pkm_paged_cache* cache, uint32_t layer_idx,
+                                    const uint32_t* bro, const uint32_t* co, int32_t batch,
+                                    int32_t buffer_length, int32_t kv_lora_rank, int32_t rope_dim,
+                                    int32_t n_out, void* k_latent, void* k_buffer,
+                                    int32_t* dev_status, int bn) {
+    DecompressArgs a{};
+    a.cache_layer = static_cast<const uint16_t*>(cache->data) +
+                    static_cast<int64_t>(layer_idx) * cache->layer_stride;
+    a.page_stride = cache->page_stride;
+    a.slot_stride = cache->slot_stride;
+    a.num_pages = cache->num_pages;
+    a.page_size = cache->page_size;
+    a.max_pages = cache->max_pages_per_seq;
+    a.page_table = cache->page_table;
+    a.row_offsets = bro;
+    a.cache_offsets = co;
+    a.batch = batch;
+    a.buffer_length = buffer_length;
+    a.kv_lora_rank = kv_lora_rank;
+    a.latent_cols = kv_lora_rank + rope_dim;
+    a.n_out = n_out;
+    a.k_latent = static_cast<uint16_t*>(k_latent);
+    a.k_buffer = static_cast<uint16_t*>(k_buffer);
+    a.status = dev_status;
+    a.timeout_ns = wait_timeout_ns();
+    a.bn = bn;
+    a.n_tiles = n_out / bn;
+    a.m_tiles = (buffer_length + 127) / 128;
+    a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
+    return a;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+extern "C" {
+
+const char* pkm_status_string(pkm_status status) {
+    switch (status) {
+        case PKM_OK: return "PKM_OK";
+        case PKM_ERR_INVALID_ARG: return "PKM_ERR_INVALID_ARG";
+        case PKM_ERR_UNSUPPORTED: return "PKM_ERR_UNSUPPORTED";
+        case PKM_ERR_CUDA: return "PKM_ERR_CUDA";
+        case PKM_ERR_OUT_OF_RANGE: return "PKM_ERR_OUT_OF_RANGE";
+        case PKM_ERR_TIMEOUT: return "PKM_ERR_TIMEOUT";
+    }
+    return "PKM_ERR_UNKNOWN";
+}
+
+pkm_status mla_decompress_k_paged(const pkm_paged_cache* cache, uint32_t layer_idx,
+                                  const uint32_t* buffer_row_offsets,
+                                  const uint32_t* cache_offsets, int32_t batch,
+                                  int32_t buffer_length, int32_t kv_lora_rank, int32_t rope_dim,
+                                  const void* w_k, int32_t n_out, void* k_latent_buffer,
+                                  void* k_buffer, int32_t* dev_status, void* stream) {
+    bool empty = false;
+    pkm_status st = check_decompress_sizes(batch, buffer_length, kv_lora_rank, rope_dim, n_out,
+                                           &empty);
+    if (st != PKM_OK || empty) return st;
+    st = check_decompress(cache, layer_idx, buffer_row_offsets, cache_offsets, batch,
+                                     buffer_length, kv_lora_rank, rope_dim, w_k, n_out,
+                                     k_latent_buffer, k_buffer);
+    if (st != PKM_OK) return st;
+    if (kv_lora_rank % 64 != 0 || kv_lora_rank > 512 || n_out % 64 != 0) return PKM_ERR_UNSUPPORTED;
+    const int bn = pick_bn(n_out);
+    DecompressArgs a = make_decompress_args(cache, layer_idx, buffer_row_offsets, cache_offsets,
+                                            batch, buffer_length, kv_lora_rank, rope_dim, n_out,
+                                            k_latent_buffer, k_buffer, dev_status, bn);
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
+    alignas(64) CUtensorMap tm_w, tm_k;
+    if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_k, kv_lora_rank, n_out,
+                   static_cast<uint64_t>(kv_lora_rank) * 2, 64, bn) ||
+        !encode_2d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_buffer, n_out, buffer_length,
+                   static_cast<uint64_t>(n_out) * 2, 64, 32))
+        return PKM_ERR_CUDA;
+    return pkm::launch_decompress_bf16(tm_w, tm_k, a, sms, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PKM_OK
+               : PKM_ERR_CUDA;
+}
+
+size_t mla_decompress_k_paged_fp8_workspace_size(int32_t buffer_length, int32_t kv_lora_rank) {
+    if (buffer_length < 0 || kv_lora_rank <= 0 || kv_lora_rank % 128 != 0) return 0;
+    const size_t L = static_cast<size_t>(buffer_length);
+    const size_t R = static_cast<size_t>(kv_lora_rank);
+    return align256(L * R) + align256(L * (R / 128) * sizeof(float));
+}
+
+pkm_status mla_decompress_k_paged_fp8(const pkm_paged_cache* cache, uint32_t layer_idx,
+                                      const uint32_t* buffer_row_offsets,
+                                      const uint32_t* cache_offsets, int32_t batch,
+                                      int32_t buffer_length, int32_t kv_lora_rank,
+                                      int32_t rope_dim, const void* w_k_e4m3,
+                                      const float* w_k_scale, int32_t n_out,
+                                      void* k_latent_buffer, void* k_buffer, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    bool empty = false;
+    pkm_status st = check_decompress_sizes(batch, buffer_length, kv_lora_rank, rope_dim, n_out,
+                                           &empty);
+    if (st != PKM_OK || empty) return st;
+    st = check_decompress(cache, layer_idx, buffer_row_offsets, cache_offsets, batch,
+                                     buffer_length, kv_lora_rank, rope_dim, w_k_e4m3, n_out,
+                                     k_latent_buffer, k_buffer);
+    if (st != PKM_OK) return st;
+    if (w_k_scale == nullptr || workspace == nullptr) return PKM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKM_ERR_INVALID_ARG;
+    if (kv_lora_rank % 128 != 0 || kv_lora_rank > 512 || n_out % 128 != 0)
+        return PKM_ERR_UNSUPPORTED;
+    if (workspace_bytes < mla_decompress_k_paged_fp8_workspace_size(buffer_length, kv_lora_rank))
+        return PKM_ERR_INVALID_ARG;
+    DecompressArgs a = make_decompress_args(cache, layer_idx, buffer_row_offsets, cache_offsets,
+                                            batch, buffer_length, kv_lora_rank, rope_dim, n_out,
+                                            k_latent_buffer, k_buffer, dev_status, 128);
+    Fp8Extra x{};
+    x.q_latent = static_cast<uint8_t*>(workspace);
+    x.q_scale = reinterpret_cast<float*>(
+        static_cast<uint8_t*>(workspace) +
+        align256(static_cast<size_t>(buffer_length) * static_cast<size_t>(kv_lora_rank)));
+    x.w_scale = w_k_scale;
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
+    alignas(64) CUtensorMap tm_q, tm_w, tm_k;
+    if (!encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.q_latent, kv_lora_rank, buffer_length,
+                   static_cast<uint64_t>(kv_lora_rank), 128, 128) ||
+        !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_k_e4m3, kv_lora_rank, n_out,
+                   static_cast<uint64_t>(kv_lora_rank), 128, 128) ||
+        !encode_2d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_buffer, n_out, buffer_length,
+                   static_cast<uint64_t>(n_out) * 2, 64, 32))
+        return PKM_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pkm::launch_fp8_gather_quantize(a, x, sms, s) != cudaSuccess) return PKM_ERR_CUDA;
+    return pkm::launch_decompress_fp8_gemm(tm_q, tm_w, tm_k, a, x, sms, s) == cudaSuccess
+               ? PKM_OK
+               : PKM_ERR_CUDA;
+}
+
+pkm_status kv_matmul_paged(const void* hidden_state, const uint32_t* input_row_offsets,
+                           int32_t batch, int32_t total_rows, int32_t k_in, const void* weight,
+                           int32_t n_out, const pkm_paged_cache* kv_cache, uint32_t layer_idx,
+                           int32_t* dev_status, void* stream) {
+    if (batch < 0 || total_rows < 0 || k_in <= 0 || n_out <= 0) return PKM_ERR_INVALID_ARG;
+    if (total_rows == 0 || batch == 0) return PKM_OK;
+    if (hidden_state == nullptr || input_row_offsets == nullptr || weight == nullptr ||
+        kv_cache == nullptr || kv_cache->data == nullptr || kv_cache->page_table == nullptr ||
+        kv_cache->cache_lengths == nullptr)
+        return PKM_ERR_INVALID_ARG;
+    if (kv_cache->num_layers <= 0 || layer_idx >= static_cast<uint32_t>(kv_cache->num_layers) ||
+        kv_cache->num_pages <= 0 || kv_cache->page_size <= 0 ||
+        kv_cache->max_pages_per_seq <= 0 || kv_cache->row_elems <= 0)
+        return PKM_ERR_INVALID_ARG;
+    const int32_t hd = kv_cache->row_elems;
+    if (n_out != hd && n_out != 2 * hd) return PKM_ERR_INVALID_ARG;
+    if (!mult8(kv_cache->layer_stride) || !mult8(kv_cache->page_stride) ||
+        !mult8(kv_cache->slot_stride) || !mult8(kv_cache->kv_stride))
+        return PKM_ERR_INVALID_ARG;
+    if (!aligned16(hidden_state) || !aligned16(weight) || !aligned16(kv_cache->data))
+        return PKM_ERR_INVALID_ARG;
+    if (k_in % 64 != 0 || hd % 64 != 0) return PKM_ERR_UNSUPPORTED;
+    KvMatmulArgs a{};
+    a.hidden = static_cast<const uint16_t*>(hidden_state);
+    a.row_offsets = input_row_offsets;
+    a.batch = batch;
+    a.total_rows = total_rows;
+    a.k_in = k_in;
+    a.n_out = n_out;
+    a.head_elems = hd;
+    a.cache_layer = static_cast<uint16_t*>(kv_cache->data) +
+                    static_cast<int64_t>(layer_idx) * kv_cache->layer_stride;
+    a.page_stride = kv_cache->page_stride;
+    a.slot_stride = kv_cache->slot_stride;
+    a.kv_stride = kv_cache->kv_stride;
+    a.num_pages = kv_cache->num_pages;
+    a.page_size = kv_cache->page_size;
+    a.max_pages = kv_cache->max_pages_per_seq;
+    a.page_table = kv_cache->page_table;
+    a.cache_lengths = kv_cache->cache_lengths;
+    a.status = dev_status;
+    a.timeout_ns = wait_timeout_ns();
+    a.bn = pick_bn(n_out);
+    a.n_tiles = n_out / a.bn;
+    a.m_tiles = (total_rows + 127) / 128;
+    a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
+    alignas(64) CUtensorMap tm_x, tm_w;
+    if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, hidden_state, k_in, total_rows,
+                   static_cast<uint64_t>(k_in) * 2, 64, 128) ||
+        !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, weight, n_out, k_in,
+                   static_cast<uint64_t>(n_out) * 2, 64, 64))
+        return PKM_ERR_CUDA;
+    return pkm::launch_kv_matmul(tm_x, tm_w, a, sms, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PKM_OK
+               : PKM_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,345 @@
+// decompress_bf16.cu -- fused paged gather + tcgen05 up-projection (bf16).
+//
+// generic_flare_mla_decompress_k_cache_ragged_paged (Modular MAX, nn/kv_cache_ragged),
+// description and Args: rows [buffer_row_offsets[b], buffer_row_offsets[b+1]) of the
+// ragged buffer receive the latent K rows of cache tokens starting at cache_offsets[b];
+// they are copied to k_latent_buffer and their first kv_lora_rank columns are multiplied
+// by W_k^T into k_buffer.
+//
+// One persistent CTA per SM walks a contiguous range of 128 x bn output tiles (tile id =
+// m_tile * n_tiles + n_tile, so a CTA revisits the same 128 latent rows for consecutive
+// n tiles and gathers them once per range segment).  Warp roles:
+//   warp 0      TMA producer: W_k tiles [bn x 64] (128-byte swizzle) into a 2-stage ring.
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (M=128, N=bn, K=16).
+//   warps 2-3   gatherers: resolve each row through buffer_row_offsets / cache_offsets /
+//               the page table, cp.async the row's nope columns straight into the
+//               swizzled A tile (one cp.async group per 64-column k-block, each signalled
+//               on its own mbarrier), and copy the full latent row to k_latent_buffer.
+//   warps 4-7   epilogue: tcgen05.ld the fp32 accumulator (TMEM double-buffered), round to
+//               bf16, stage in swizzled shared memory, TMA-store 32 x 64 boxes of k_buffer.
+// The A tile (128 rows x kv_lora_rank) stays resident in shared memory for every n tile
+// of its segment; the MMA of a tile overlaps the epilogue of the previous one.
+#include "pkm_device.cuh"
+#include "pkm_internal.h"
+
+namespace pkm {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBM = 128;
+constexpr int kKBMax = 8;                    // kv_lora_rank <= 512 = 8 k-blocks of 64
+constexpr int kABlockBytes = kBM * 128;      // 16 KB per k-block
+constexpr int kStages = 2;
+constexpr int kBStageBytes = 256 * 128;      // bn <= 256 rows of 128 bytes
+constexpr int kEpiWarps = 4;
+constexpr int kOutBufBytes = 32 * 128;       // 32 rows x 64 bf16
+constexpr int kGatherThreads = 64;
+constexpr uint32_t kTmemCols = 512;
+
+struct Bars {
+    uint64_t b_full[kStages];
+    uint64_t b_empty[kStages];
+    uint64_t a_full[kKBMax];
+    uint64_t a_empty;
+    uint64_t t_full[2];
+    uint64_t t_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+    int gather_go;
+};
+
+constexpr size_t kOffA = 0;
+constexpr size_t kOffB = kOffA + size_t(kKBMax) * kABlockBytes;
+constexpr size_t kOffOut = kOffB + size_t(kStages) * kBStageBytes;
+constexpr size_t kOffRows = kOffOut + size_t(kEpiWarps) * 2 * kOutBufBytes;
+constexpr size_t kOffBars = kOffRows + kBM * sizeof(int64_t);
+constexpr size_t kSmemBytes = kOffBars + sizeof(Bars) + 1024;  // + base alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decompress_bf16_kernel(const __grid_constant__ CUtensorMap tm_w,
+                           const __grid_constant__ CUtensorMap tm_kbuf, const DecompressArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem + kOffA;
+    uint8_t* sB = smem + kOffB;
+    uint8_t* sOut = smem + kOffOut;
+    int64_t* s_rows = reinterpret_cast<int64_t*>(smem + kOffRows);
+    Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int KB = a.kv_lora_rank / 64;
+    const int bn = a.bn;
+    const int64_t T = a.total_tiles;
+    const int64_t G = gridDim.x;
+    const int64_t t_begin = T * blockIdx.x / G;
+    const int64_t t_end = T * (blockIdx.x + 1) / G;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars->b_full[s], 1);
+            mbar_init(&bars->b_empty[s], 1);
+        }
+        for (int kb = 0; kb < kKBMax; ++kb) mbar_init(&bars->a_full[kb], kGatherThreads);
+        mbar_init(&bars->a_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->t_full[i], 1);
+            mbar_init(&bars->t_empty[i], kEpiWarps);
+        }
+        mbar_init(&bars->mma_done, 1);
+        bars->abort_flag = 0;
+        bars->gather_go = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tm_w);
+        tma_prefetch_map(&tm_kbuf);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const WaitCtl wc{&bars->abort_flag, a.status, a.timeout_ns};
+    const int64_t row_end = decompress_row_end(a);
+
+    if (warp == 0) {
+        // ---------------- W_k producer ----------------
+        if (lane == 0) {
+            const uint64_t keep = policy_evict_last();
+            uint32_t it = 0;
+            bool issued[kStages] = {false, false};
+            uint32_t last_phase[kStages] = {0, 0};
+            bool ok = true;
+            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+                const int n = static_cast<int>(t % a.n_tiles);
+                for (int kb = 0; kb < KB; ++kb) {
+                    const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+                    if (!mbar_wait(&bars->b_empty[s], ph ^ 1, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars->b_full[s], static_cast<uint32_t>(bn) * 128);
+                    tma_load_2d_hint(sB + s * kBStageBytes, &tm_w, &bars->b_full[s], kb * 64,
+                                     n * bn, keep);
+                    issued[s] = true;
+                    last_phase[s] = ph;
+                    ++it;
+                }
+            }
+            if (!ok) {  // let loads already in flight land before the CTA retires
+                for (int s = 0; s < kStages; ++s)
+                    if (issued[s]) mbar_wait(&bars->b_full[s], last_phase[s], wc, false);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(128, bn, false, false);
+            uint32_t it = 0, tile_i = 0, seg = 0;
+            int64_t cur_m = -1;
+            bool ok = true;
+            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+                const int64_t m = t / a.n_tiles;
+                const bool new_seg = (m != cur_m);
+                if (new_seg) {
+                    if (cur_m >= 0) {
+                        mma_commit(&bars->a_empty);  // sA free once these MMAs retire
+                        ++seg;
+                    }
+                    cur_m = m;
+                }
+                const uint32_t acc = tile_i & 1, aph = (tile_i >> 1) & 1;
+                if (!mbar_wait(&bars->t_empty[acc], aph ^ 1, wc)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + acc * static_cast<uint32_t>(bn);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (new_seg && !mbar_wait(&bars->a_full[kb], seg & 1, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+                    if (!mbar_wait(&bars->b_full[s], ph, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sA + kb * kABlockBytes);
+                    const uint32_t b_addr = smem_u32(sB + s * kBStageBytes);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(d, sdesc_sw128(a_addr + k * 32, 16, 1024),
+                                 sdesc_sw128(b_addr + k * 32, 16, 1024), idesc,
+                                 (kb | k) != 0 ? 1u : 0u);
+                    mma_commit(&bars->b_empty[s]);
+                    ++it;
+                }
+                if (!ok) break;
+                mma_commit(&bars->t_full[acc]);
+                ++tile_i;
+            }
+            mma_commit(&bars->mma_done);
+            mbar_wait(&bars->mma_done, 0, wc, false);
+        }
+    } else if (warp < 4) {
+        // ---------------- gatherers ----------------
+        const int g = threadIdx.x - 64;
+        const int chunk = g & 7;   // 16-byte chunk inside a 128-byte k-block row
+        const int rsub = g >> 3;   // row phase 0..7
+        const int cchunks = a.latent_cols / 8;
+        uint32_t seg = 0;
+        int64_t cur_m = -1;
+        for (int64_t t = t_begin; t < t_end; ++t) {
+            const int64_t m = t / a.n_tiles;
+            if (m == cur_m) continue;
+            cur_m = m;
+            const bool writer = (t % a.n_tiles) == 0;  // this CTA owns tile (m, 0)
+            for (int i = g; i < kBM; i += kGatherThreads) {
+                const int64_t off = decompress_row_source(a, m * kBM + i, row_end);
+                if (off == -2) report(a.status, PKM_ERR_OUT_OF_RANGE);
+                s_rows[i] = off;
+            }
+            if (g == 0)
+                bars->gather_go =
+                    (seg == 0 || mbar_wait(&bars->a_empty, (seg - 1) & 1, wc)) ? 1 : 0;
+            named_bar_sync(1, kGatherThreads);
+            if (!bars->gather_go) break;
+            for (int kb = 0; kb < KB; ++kb) {
+                const uint32_t base = smem_u32(sA + kb * kABlockBytes);
+#pragma unroll 4
+                for (int j = 0; j < kBM / 8; ++j) {
+                    const int row = rsub + 8 * j;
+                    const int64_t off = s_rows[row];
+                    const uint16_t* src =
+                        off >= 0 ? a.cache_layer + off + kb * 64 + chunk * 8 : a.cache_layer;
+                    cp_async_16(base + row * 128 + ((chunk ^ (row & 7)) << 4), src,
+                                off >= 0 ? 16u : 0u);
+                }
+                cp_async_commit();
+            }
+            for (int kb = 0; kb < KB; ++kb) {
+                cp_async_wait_dyn(KB - 1 - kb);
+                fence_proxy_async_smem();
+                mbar_arrive(&bars->a_full[kb]);
+            }
+            if (writer) {
+                const int total = kBM * cchunks;
+                for (int i0 = g; i0 < total; i0 += 4 * kGatherThreads) {
+                    uint4 v[4];
+                    int64_t dst[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int idx = i0 + u * kGatherThreads;
+                        dst[u] = -1;
+                        if (idx < total) {
+                            const int row = idx / cchunks;
+                            const int c = idx - row * cchunks;
+                            const int64_t off = s_rows[row];
+                            if (off >= 0) {
+                                v[u] = ld_nc_v4(a.cache_layer + off + c * 8);
+                                dst[u] = (m * kBM + row) * a.latent_cols + c * 8;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (dst[u] >= 0) st_v4(a.k_latent + dst[u], v[u]);
+                }
+            }
+            named_bar_sync(1, kGatherThreads);
+            ++seg;
+        }
+        cp_async_wait<0>();
+    } else {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;  // TMEM lane quarter == 32-row slab of the tile
+        uint32_t tile_i = 0, st_i = 0;
+        int64_t cur_m = -1, my_row = 0;
+        bool slab_full = false, my_valid = false;
+        for (int64_t t = t_begin; t < t_end; ++t) {
+            const int64_t m = t / a.n_tiles;
+            const int n = static_cast<int>(t % a.n_tiles);
+            if (m != cur_m) {
+                cur_m = m;
+                my_row = m * kBM + q * 32 + lane;
+                my_valid = decompress_row_source(a, my_row, row_end) >= 0;
+                slab_full = __all_sync(0xffffffffu, my_valid);
+            }
+            const uint32_t acc = tile_i & 1, ph = (tile_i >> 1) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->t_full[acc], ph, wc))) break;
+            tc_fence_after();
+            const uint32_t tbase =
+                tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(bn);
+            for (int c = 0; c < bn / 64; ++c) {
+                uint32_t v0[32], v1[32];
+                tmem_ld_x32(tbase + c * 64, v0);
+                tmem_ld_x32(tbase + c * 64 + 32, v1);
+                tmem_ld_wait();
+                uint32_t p[32];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    p[j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
+                    p[16 + j] =
+                        pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
+                }
+                if (slab_full) {
+                    uint8_t* stage = sOut + (q * 2 + (st_i & 1)) * kOutBufBytes;
+                    if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer
+                    __syncwarp();
+                    const uint32_t rowaddr = smem_u32(stage) + lane * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(rowaddr + ((j ^ (lane & 7)) << 4), p[4 * j], p[4 * j + 1],
+                                     p[4 * j + 2], p[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_kbuf, stage, n * bn + c * 64,
+                                     static_cast<int32_t>(m * kBM + q * 32));
+                        bulk_commit();
+                    }
+                    ++st_i;
+                } else if (my_valid) {  // slab with uncovered rows: plain per-row stores
+                    uint16_t* dst = a.k_buffer + my_row * a.n_out + n * bn + c * 64;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_v4(dst + j * 8,
+                              make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->t_empty[acc]);
+            ++tile_i;
+        }
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_decompress_bf16(const CUtensorMap& tm_w, const CUtensorMap& tm_kbuf,
+                                   DecompressArgs args, int num_sms, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(decompress_bf16_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    const int64_t grid = args.total_tiles < num_sms ? args.total_tiles : num_sms;
+    decompress_bf16_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
+        tm_w, tm_kbuf, args);
+    return cudaGetLastError();
+}
+
+}  // namespace pkm

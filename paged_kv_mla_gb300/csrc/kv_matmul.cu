@@ -1,0 +1,260 @@
+// kv_matmul.cu -- ragged GEMM written into the paged K/V cache.
+//
+// kv_matmul_ragged_paged (Modular MAX, nn/kv_cache_ragged), description and Args: Y =
+// hidden_state [sum(seq_lens), num_heads*head_size] x weight [num_heads*head_size,
+// num_kv_heads*head_size]; row i of request b is written into the cache of layer
+// layer_idx at position cache_lengths[b] + i.  The output columns are split K then V
+// (head_elems each).
+//
+// Persistent CTAs over 128 x bn tiles.  Warp 0 streams A (hidden_state, K-major, box
+// 64 x 128) and B (weight, N contiguous = MN-major, bn/64 boxes of 64 x 64) with TMA into
+// a 4-stage ring; warp 1 issues tcgen05.mma (B described as MN-major, 128-byte swizzle);
+// warps 2-5 drain the double-buffered TMEM accumulator, round to bf16, and scatter each
+// row's 64-column chunk to its (page, slot) with 16-byte stores, 4 full rows of 128 bytes
+// per warp instruction.
+#include "pkm_device.cuh"
+#include "pkm_internal.h"
+
+namespace pkm {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;
+constexpr int kStages = 4;
+constexpr int kAStageBytes = kBM * 128;       // 128 rows x 64 bf16
+constexpr int kBStageBytes = 4 * 64 * 128;    // up to 4 boxes of 64 k-rows x 64 n
+constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+constexpr int kEpiWarps = 4;
+constexpr int kOutBufBytes = 32 * 128;
+constexpr uint32_t kTmemCols = 512;
+
+struct Bars {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t t_full[2];
+    uint64_t t_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+constexpr size_t kOffStages = 0;
+constexpr size_t kOffOut = kOffStages + size_t(kStages) * kStageBytes;
+constexpr size_t kOffBars = kOffOut + size_t(kEpiWarps) * kOutBufBytes;
+constexpr size_t kSmemBytes = kOffBars + sizeof(Bars) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
+
+// Element offset (inside the layer's K plane) of the slot that receives row r, -1 when no
+// request covers r, -2 when the position resolves past the page table or the cache.
+__device__ __forceinline__ int64_t kv_row_dest(const KvMatmulArgs& a, int64_t r) {
+    const uint32_t* iro = a.row_offsets;
+    const int64_t covered = static_cast<int64_t>(__ldg(iro + a.batch));
+    if (r >= a.total_rows || r >= covered) return -1;
+    if (static_cast<uint64_t>(r) < static_cast<uint64_t>(__ldg(iro))) return -1;
+    int lo = 0, hi = a.batch;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<uint64_t>(__ldg(iro + mid)) <= static_cast<uint64_t>(r)) lo = mid;
+        else hi = mid;
+    }
+    const uint64_t pos = static_cast<uint64_t>(__ldg(a.cache_lengths + lo)) +
+                         (static_cast<uint64_t>(r) - __ldg(iro + lo));
+    const uint64_t lp = pos / static_cast<uint64_t>(a.page_size);
+    if (lp >= static_cast<uint64_t>(a.max_pages)) return -2;
+    const uint32_t page = __ldg(a.page_table + static_cast<int64_t>(lo) * a.max_pages + lp);
+    if (page >= static_cast<uint32_t>(a.num_pages)) return -2;
+    return static_cast<int64_t>(page) * a.page_stride +
+           static_cast<int64_t>(pos % static_cast<uint64_t>(a.page_size)) * a.slot_stride;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    kv_matmul_kernel(const __grid_constant__ CUtensorMap tm_x,
+                     const __grid_constant__ CUtensorMap tm_w, const KvMatmulArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sStages = smem + kOffStages;
+    uint8_t* sOut = smem + kOffOut;
+    Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bn = a.bn;
+    const int KB = a.k_in / 64;
+    const int64_t T = a.total_tiles;
+    const int64_t G = gridDim.x;
+    const int64_t t_begin = T * blockIdx.x / G;
+    const int64_t t_end = T * (blockIdx.x + 1) / G;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->t_full[i], 1);
+            mbar_init(&bars->t_empty[i], kEpiWarps);
+        }
+        mbar_init(&bars->mma_done, 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tm_x);
+        tma_prefetch_map(&tm_w);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const WaitCtl wc{&bars->abort_flag, a.status, a.timeout_ns};
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t keep = policy_evict_last();
+            const uint32_t stage_tx = kAStageBytes + static_cast<uint32_t>(bn) * 128;
+            uint32_t it = 0;
+            bool issued[kStages] = {};
+            uint32_t last_phase[kStages] = {};
+            bool ok = true;
+            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+                const int64_t m = t / a.n_tiles;
+                const int n = static_cast<int>(t % a.n_tiles);
+                for (int kb = 0; kb < KB; ++kb) {
+                    const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+                    if (!mbar_wait(&bars->empty[s], ph ^ 1, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = sStages + s * kStageBytes;
+                    mbar_arrive_expect_tx(&bars->full[s], stage_tx);
+                    tma_load_2d(st, &tm_x, &bars->full[s], kb * 64, static_cast<int32_t>(m * kBM));
+                    for (int j = 0; j < bn / 64; ++j)
+                        tma_load_2d_hint(st + kAStageBytes + j * 8192, &tm_w, &bars->full[s],
+                                         n * bn + j * 64, kb * 64, keep);
+                    issued[s] = true;
+                    last_phase[s] = ph;
+                    ++it;
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < kStages; ++s)
+                    if (issued[s]) mbar_wait(&bars->full[s], last_phase[s], wc, false);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(128, bn, false, true);
+            uint32_t it = 0, tile_i = 0;
+            bool ok = true;
+            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+                const uint32_t acc = tile_i & 1, aph = (tile_i >> 1) & 1;
+                if (!mbar_wait(&bars->t_empty[acc], aph ^ 1, wc)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + acc * static_cast<uint32_t>(bn);
+                for (int kb = 0; kb < KB; ++kb) {
+                    const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+                    if (!mbar_wait(&bars->full[s], ph, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sStages + s * kStageBytes);
+                    const uint32_t b_addr = a_addr + kAStageBytes;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(d, sdesc_sw128(a_addr + k * 32, 16, 1024),
+                                 sdesc_sw128(b_addr + k * 2048, 8192, 1024), idesc,
+                                 (kb | k) != 0 ? 1u : 0u);
+                    mma_commit(&bars->empty[s]);
+                    ++it;
+                }
+                if (!ok) break;
+                mma_commit(&bars->t_full[acc]);
+                ++tile_i;
+            }
+            mma_commit(&bars->mma_done);
+            mbar_wait(&bars->mma_done, 0, wc, false);
+        }
+    } else {
+        const int q = warp & 3;
+        uint8_t* stage = sOut + q * kOutBufBytes;
+        const uint32_t stage_addr = smem_u32(stage);
+        uint32_t tile_i = 0;
+        int64_t cur_m = -1, my_dst = -1;
+        for (int64_t t = t_begin; t < t_end; ++t) {
+            const int64_t m = t / a.n_tiles;
+            const int n = static_cast<int>(t % a.n_tiles);
+            if (m != cur_m) {
+                cur_m = m;
+                my_dst = kv_row_dest(a, m * kBM + q * 32 + lane);
+                if (my_dst == -2) report(a.status, PKM_ERR_OUT_OF_RANGE);
+            }
+            const uint32_t acc = tile_i & 1, ph = (tile_i >> 1) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->t_full[acc], ph, wc))) break;
+            tc_fence_after();
+            const uint32_t tbase =
+                tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(bn);
+            for (int c = 0; c < bn / 64; ++c) {
+                uint32_t v0[32], v1[32];
+                tmem_ld_x32(tbase + c * 64, v0);
+                tmem_ld_x32(tbase + c * 64 + 32, v1);
+                tmem_ld_wait();
+                uint32_t p[32];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    p[j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
+                    p[16 + j] =
+                        pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
+                }
+                const uint32_t rowaddr = stage_addr + lane * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(rowaddr + ((j ^ (lane & 7)) << 4), p[4 * j], p[4 * j + 1],
+                                 p[4 * j + 2], p[4 * j + 3]);
+                __syncwarp();
+                // 64 output columns of one chunk lie entirely in the K or the V plane
+                const int col0 = n * bn + c * 64;
+                const int64_t plane = col0 < a.head_elems ? 0 : a.kv_stride;
+                const int colp = (col0 < a.head_elems ? col0 : col0 - a.head_elems) + (lane & 7) * 8;
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int row = it * 4 + (lane >> 3);
+                    const int64_t dst = __shfl_sync(0xffffffffu, my_dst, row);
+                    const uint4 v = ld_shared_v4(stage_addr + row * 128 + (((lane & 7) ^ (row & 7)) << 4));
+                    if (dst >= 0) st_v4(a.cache_layer + plane + dst + colp, v);
+                }
+                __syncwarp();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->t_empty[acc]);
+            ++tile_i;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_kv_matmul(const CUtensorMap& tm_x, const CUtensorMap& tm_w, KvMatmulArgs args,
+                             int num_sms, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(kv_matmul_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    const int64_t grid = args.total_tiles < num_sms ? args.total_tiles : num_sms;
+    kv_matmul_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tm_x, tm_w,
+                                                                                    args);
+    return cudaGetLastError();
+}
+
+}  // namespace pkm

@@ -1,0 +1,109 @@
+// pkm_internal.h -- argument blocks passed from the C entry points (api.cu) to the kernel
+// launchers (decompress_bf16.cu, decompress_fp8.cu, kv_matmul.cu).  Not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace pkm {
+
+// One decompress problem, already validated on the host.  Pointers are device memory.
+struct DecompressArgs {
+    const uint16_t* cache_layer;   // cache data + layer_idx * layer_stride (bf16)
+    int64_t page_stride;           // elements
+    int64_t slot_stride;           // elements
+    int32_t num_pages;
+    int32_t page_size;
+    int32_t max_pages;             // page-table row length
+    const uint32_t* page_table;    // [batch, max_pages]
+    const uint32_t* row_offsets;   // buffer_row_offsets [batch + 1]
+    const uint32_t* cache_offsets; // [>= batch]
+    int32_t batch;
+    int32_t buffer_length;         // rows of the outputs
+    int32_t kv_lora_rank;          // R
+    int32_t latent_cols;           // C = R + rope
+    int32_t n_out;                 // N
+    uint16_t* k_latent;            // [L, C] bf16
+    uint16_t* k_buffer;            // [L, N] bf16
+    int32_t* status;               // nullable
+    uint64_t timeout_ns;
+    // tiling, filled by the launcher
+    int32_t bn;                    // N tile
+    int32_t n_tiles;               // N / bn
+    int32_t m_tiles;               // ceil(L / 128)
+    int64_t total_tiles;           // m_tiles * n_tiles
+};
+
+struct Fp8Extra {
+    uint8_t* q_latent;             // [L, R] e4m3 (workspace)
+    float* q_scale;                // [L, R/128] (workspace)
+    const float* w_scale;          // [N/128, R/128]
+};
+
+// One kv_matmul problem, already validated.
+struct KvMatmulArgs {
+    const uint16_t* hidden;        // [M, K] bf16
+    const uint32_t* row_offsets;   // input_row_offsets [batch + 1]
+    int32_t batch;
+    int32_t total_rows;            // M
+    int32_t k_in;                  // K
+    int32_t n_out;                 // N = HD or 2 HD
+    int32_t head_elems;            // HD
+    uint16_t* cache_layer;         // cache data + layer_idx * layer_stride
+    int64_t page_stride, slot_stride, kv_stride;
+    int32_t num_pages, page_size, max_pages;
+    const uint32_t* page_table;
+    const uint32_t* cache_lengths;
+    int32_t* status;
+    uint64_t timeout_ns;
+    int32_t bn, n_tiles, m_tiles;
+    int64_t total_tiles;
+};
+
+// Launchers (return a CUDA error code; 0 = success).  Tensor maps are encoded by the
+// caller.
+cudaError_t launch_decompress_bf16(const CUtensorMap& tm_w, const CUtensorMap& tm_kbuf,
+                                   DecompressArgs args, int num_sms, cudaStream_t stream);
+cudaError_t launch_fp8_gather_quantize(DecompressArgs args, Fp8Extra extra, int num_sms,
+                                       cudaStream_t stream);
+cudaError_t launch_decompress_fp8_gemm(const CUtensorMap& tm_q, const CUtensorMap& tm_w,
+                                       const CUtensorMap& tm_kbuf, DecompressArgs args,
+                                       Fp8Extra extra, int num_sms, cudaStream_t stream);
+cudaError_t launch_kv_matmul(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
+                             KvMatmulArgs args, int num_sms, cudaStream_t stream);
+
+// Row bookkeeping shared by the decompress kernels: element offset (inside the layer) of
+// the cache slot that feeds output row r, -1 when no request covers r (or r >= row_end),
+// -2 when the token resolves past the page-table row or to a page id >= num_pages.
+// The request of r is the largest b with row_offsets[b] <= r (row_offsets non-decreasing,
+// so empty requests are skipped); its token is cache_offsets[b] + r - row_offsets[b].
+__device__ __forceinline__ int64_t decompress_row_source(const DecompressArgs& a, int64_t r,
+                                                         int64_t row_end) {
+    if (r >= row_end) return -1;
+    const uint32_t* bro = a.row_offsets;
+    if (static_cast<uint64_t>(r) < static_cast<uint64_t>(__ldg(bro))) return -1;
+    int lo = 0, hi = a.batch;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<uint64_t>(__ldg(bro + mid)) <= static_cast<uint64_t>(r)) lo = mid;
+        else hi = mid;
+    }
+    const uint64_t i = static_cast<uint64_t>(r) - __ldg(bro + lo);
+    const uint64_t t = static_cast<uint64_t>(__ldg(a.cache_offsets + lo)) + i;
+    const uint64_t lp = t / static_cast<uint64_t>(a.page_size);
+    if (lp >= static_cast<uint64_t>(a.max_pages)) return -2;
+    const uint32_t page = __ldg(a.page_table + static_cast<int64_t>(lo) * a.max_pages + lp);
+    if (page >= static_cast<uint32_t>(a.num_pages)) return -2;
+    return static_cast<int64_t>(page) * a.page_stride +
+           static_cast<int64_t>(t % static_cast<uint64_t>(a.page_size)) * a.slot_stride;
+}
+
+// min(buffer_length, row_offsets[batch]): rows at or past it are not written.
+__device__ __forceinline__ int64_t decompress_row_end(const DecompressArgs& a) {
+    const int64_t covered = static_cast<int64_t>(__ldg(a.row_offsets + a.batch));
+    return covered < a.buffer_length ? covered : a.buffer_length;
+}
+
+}  // namespace pkm

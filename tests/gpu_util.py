@@ -1,0 +1,129 @@
+"""Device-side helpers for the GPU tests: move a workload to cuda:0, call the library
+through its Python binding (which calls the C ABI), and bring results back as numpy bit
+patterns for comparison with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from workloads import SENTINEL_OUT, DecompressInputs, KvMatmulInputs
+
+BF16_TOL = (1e-2, 2e-3)   # |gpu - ref| <= rtol * |ref| + atol, bf16 in / fp32 accumulate
+FP8_TOL = (3e-2, 5e-3)    # same form, FP8 path against the dequantised-value oracle
+
+
+def _i16(v: int) -> int:
+    return v - 65536 if v >= 32768 else v
+
+
+def dev(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """numpy array -> device tensor with the same bytes (uint16 travels as int16, uint32 as
+    int32)."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    elif a.dtype == np.uint32:
+        a = a.view(np.int32)
+    return torch.from_numpy(a).to(device)
+
+
+def host_u16(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().numpy().view(np.uint16)
+
+
+def bf16_f64(a) -> np.ndarray:
+    return (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def assert_close_bf16(got_bits, ref_bits, tol, what=""):
+    g = bf16_f64(got_bits)
+    r = bf16_f64(ref_bits)
+    rtol, atol = tol
+    err = np.abs(g - r)
+    bad = ~(err <= rtol * np.abs(r) + atol)
+    if bad.any():
+        idx = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements outside tolerance; "
+                             f"first at {tuple(idx)}: gpu {g[tuple(idx)]} oracle {r[tuple(idx)]}")
+
+
+class DeviceDecompress:
+    """A DecompressInputs problem resident on the GPU, with sentinel-filled outputs."""
+
+    def __init__(self, d: DecompressInputs, fp8: bool = False):
+        import paged_kv_mla_gb300 as pkm
+        self.d = d
+        self.cache = dev(d.cache)
+        self.pt = dev(d.page_table)
+        self.bro = dev(d.buffer_row_offsets)
+        self.co = dev(d.cache_offsets)
+        ls, ps, ss = d.strides
+        self.pc = pkm.PagedCache(data=self.cache, page_table=self.pt, layer_stride=ls,
+                                 page_stride=ps, slot_stride=ss, num_layers=d.num_layers,
+                                 num_pages=d.num_pages, page_size=d.page_size,
+                                 row_elems=d.latent_cols)
+        L = max(d.buffer_length, 1)
+        self.k_latent = torch.full((L, d.latent_cols), _i16(SENTINEL_OUT), dtype=torch.int16,
+                                   device="cuda")
+        self.k_buffer = torch.full((L, d.n_out), _i16(SENTINEL_OUT), dtype=torch.int16,
+                                   device="cuda")
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.fp8 = fp8
+        if fp8:
+            self.w = dev(d.w_k_e4m3)
+            self.w_scale = dev(d.w_k_scale)
+            nbytes = pkm.mla_decompress_k_paged_fp8_workspace_size(d.buffer_length, d.kv_lora_rank)
+            self.workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+        else:
+            self.w = dev(d.w_k)
+
+    def run(self, stream=None, check=True):
+        import paged_kv_mla_gb300 as pkm
+        d = self.d
+        if self.fp8:
+            return pkm.mla_decompress_k_paged_fp8(
+                self.pc, d.layer_idx, self.bro, self.co, d.buffer_length, d.kv_lora_rank,
+                d.rope_dim, self.w, self.w_scale, self.k_latent, self.k_buffer, self.workspace,
+                dev_status=self.status, stream=stream, check=check)
+        return pkm.mla_decompress_k_paged(self.pc, d.layer_idx, self.bro, self.co, d.buffer_length,
+                                          d.kv_lora_rank, d.rope_dim, self.w, self.k_latent,
+                                          self.k_buffer, dev_status=self.status, stream=stream,
+                                          check=check)
+
+    def results(self):
+        torch.cuda.synchronize()
+        L = self.d.buffer_length
+        return (host_u16(self.k_latent)[:L], host_u16(self.k_buffer)[:L],
+                int(self.status.item()))
+
+    def fp8_workspace(self):
+        import paged_kv_mla_gb300 as pkm
+        q, s = pkm.fp8_workspace_views(self.workspace, self.d.buffer_length, self.d.kv_lora_rank)
+        return q.cpu().numpy(), s.cpu().numpy()
+
+
+class DeviceKvMatmul:
+    def __init__(self, k: KvMatmulInputs):
+        import paged_kv_mla_gb300 as pkm
+        self.k = k
+        self.hidden = dev(k.hidden_state)
+        self.iro = dev(k.input_row_offsets)
+        self.weight = dev(k.weight)
+        self.cache = dev(k.cache)
+        self.pt = dev(k.page_table)
+        self.cl = dev(k.cache_lengths)
+        ls, ps, ss, kvs = k.strides
+        self.pc = pkm.PagedCache(data=self.cache, page_table=self.pt, layer_stride=ls,
+                                 page_stride=ps, slot_stride=ss, num_layers=k.cache.shape[0],
+                                 num_pages=k.num_pages, page_size=k.page_size,
+                                 row_elems=k.head_elems, kv_stride=kvs, cache_lengths=self.cl)
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def run(self, stream=None, check=True):
+        import paged_kv_mla_gb300 as pkm
+        return pkm.kv_matmul_paged(self.hidden, self.iro, self.weight, self.pc, self.k.layer_idx,
+                                   dev_status=self.status, stream=stream, check=check)
+
+    def results(self):
+        torch.cuda.synchronize()
+        return host_u16(self.cache).reshape(self.k.cache.shape), int(self.status.item())

@@ -1,0 +1,109 @@
+"""The C-ABI library builds, loads without a GPU, exports every function include/*.h
+declares, and rejects invalid calls on the host (before any CUDA call).  No GPU."""
+from __future__ import annotations
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_mla_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                            text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["mla_decompress_k_paged", "mla_decompress_k_paged_fp8",
+              "mla_decompress_k_paged_fp8_workspace_size", "kv_matmul_paged", "pkm_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_status_strings(lib):
+    lib.pkm_status_string.restype = ctypes.c_char_p
+    assert lib.pkm_status_string(0) == b"PKM_OK"
+    assert lib.pkm_status_string(4) == b"PKM_ERR_OUT_OF_RANGE"
+    assert lib.pkm_status_string(99) == b"PKM_ERR_UNKNOWN"
+
+
+def test_workspace_size(lib):
+    f = lib.mla_decompress_k_paged_fp8_workspace_size
+    f.restype = ctypes.c_size_t
+    assert f(1000, 512) == 512000 + (1000 * 4 * 4 + 255) // 256 * 256
+    assert f(1000, 500) == 0 and f(-1, 512) == 0
+    assert f(0, 512) == 0
+
+
+def _cache(pkm, **kw):
+    import torch
+    base = dict(data=torch.zeros(4096, dtype=torch.int16), page_table=torch.zeros(8, dtype=torch.int32),
+                layer_stride=2048, page_stride=16 * 80, slot_stride=80, num_layers=1, num_pages=1,
+                page_size=16, row_elems=80)
+    base.update(kw)
+    return pkm.PagedCache(**base)
+
+
+def test_invalid_calls_return_status_without_a_gpu(lib):
+    import torch
+    import paged_kv_mla_gb300 as pkm
+    t16 = torch.zeros(1024, dtype=torch.int16)
+    bro = torch.tensor([0, 4], dtype=torch.int32)
+    co = torch.zeros(2, dtype=torch.int32)
+    w = torch.zeros(64 * 64, dtype=torch.int16).view(64, 64)
+
+    def call(cache, L=4, R=64, P=16, w=w, lat=t16, kb=t16, bro=bro):
+        return pkm.mla_decompress_k_paged(cache, 0, bro, co, L, R, P, w, lat, kb, stream=0,
+                                          check=False)
+
+    good = _cache(pkm)
+    assert call(good, R=60, P=20) == pkm.PKM_ERR_UNSUPPORTED          # R not a multiple of 64
+    assert call(good, R=576, P=0) != pkm.PKM_OK                        # row_elems mismatch
+    assert call(_cache(pkm, row_elems=81), P=17) == pkm.PKM_ERR_UNSUPPORTED  # 81*2 B rows
+    assert call(_cache(pkm, slot_stride=81)) == pkm.PKM_ERR_INVALID_ARG  # 16-byte rule
+    assert call(_cache(pkm, num_pages=0)) == pkm.PKM_ERR_INVALID_ARG
+    assert call(good, L=-1) == pkm.PKM_ERR_INVALID_ARG
+    assert call(good, L=0) == pkm.PKM_OK                               # nothing to do
+    assert call(good, lat=t16[1:]) == pkm.PKM_ERR_INVALID_ARG          # misaligned output
+    r = pkm.kv_matmul_paged(torch.zeros(4, 100, dtype=torch.int16), bro, torch.zeros(100, 128, dtype=torch.int16),
+                            _cache(pkm, row_elems=128, cache_lengths=co), 0, stream=0, check=False)
+    assert r == pkm.PKM_ERR_UNSUPPORTED                                # k_in not a multiple of 64
+    r = pkm.kv_matmul_paged(torch.zeros(4, 128, dtype=torch.int16), bro, torch.zeros(128, 96, dtype=torch.int16),
+                            _cache(pkm, row_elems=128, cache_lengths=co), 0, stream=0, check=False)
+    assert r == pkm.PKM_ERR_INVALID_ARG                                # n_out not HD or 2 HD
+    r = pkm.kv_matmul_paged(torch.zeros(4, 128, dtype=torch.int16), bro, torch.zeros(128, 128, dtype=torch.int16),
+                            _cache(pkm, row_elems=128), 0, stream=0, check=False)
+    assert r == pkm.PKM_ERR_INVALID_ARG                                # cache_lengths missing
+    with pytest.raises(pkm.PkmError):
+        pkm.mla_decompress_k_paged(good, 0, bro, co, 4, 60, 20, w, t16, t16, stream=0)
+
+
+def test_oracle_and_product_share_no_code():
+    """The oracle is test infrastructure: the CUDA sources never include or name it, and it
+    never includes the library's headers."""
+    for f in glob.glob(os.path.join(ROOT, "paged_kv_mla_gb300", "**", "*"), recursive=True):
+        if f.endswith((".cu", ".cuh", ".h", ".py")):
+            assert "oracle" not in open(f).read().lower(), f
+    src = open(os.path.join(ROOT, "oracle", "pkm_oracle.c")).read()
+    assert "#include \"" not in src and "paged_kv_mla" not in src

@@ -406,3 +406,15 @@ def test_kv_matmul_then_decompress_composes():
     assert_correctly_rounded_bf16(lat, yx)
     exact = bf16_to_f64(lat[:, :512]) @ bf16_to_f64(d.w_k).T
     assert_correctly_rounded_bf16(kb, exact)
+
+
+def test_kv_row_dest_matches_worked_example():
+    with open(os.path.join(GOLDEN, "kv_matmul_worked_example.json")) as f:
+        ex = json.load(f)
+    ps, P, HD = ex["page_size"], ex["num_pages"], ex["head_elems"]
+    view = oracle.PagedCacheView(np.zeros(2 * P * ps * HD, np.uint16), 2 * P * ps * HD, ps * HD, HD,
+                                 P, ps, np.array(ex["page_table"], np.uint32), 2, kv_stride=P * ps * HD)
+    dest = oracle.kv_row_dest(np.array(ex["input_row_offsets"], np.uint32), 2, 3,
+                              np.array(ex["cache_lengths"], np.uint32), view)
+    k_writes = [w for w in ex["expected_writes"] if w["plane"] == "K"]
+    assert list(dest) == [w["page"] * ps * HD + w["slot"] * HD for w in k_writes]
