@@ -1,0 +1,454 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV MLA hot path on GB300.
+
+Default workload (one step = one call of mla_decompress_k_paged): the DeepSeek-V3-shaped
+bf16 decompress (16 requests, lengths ~U[512, 4096], cache_offsets ~U[0, len/4],
+page_size 128, kv_lora_rank 512 + rope 64, W_k [16384, 512]), seeded synthetic data.
+The headline value is decompress TFLOP/s (2 * rows * 512 * 16384 per step); the same line
+carries rows/s, the roofline of the kernel, the FP8 decompress, the long-context
+decompress and kv_matmul (TFLOP/s and GB/s), an end-to-end number with host buffers, and
+the CPU oracle timed on this host.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 is launched by torchrun: each rank runs its own replica of the workload (weak
+scaling, no collective on the data path); timing is the max over ranks.
+--impl reference times the CPU oracle (the only other implementation of this method) on a
+bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA K-decompress TFLOP/s & rows/s (% of GB300 tensor peak); kv_matmul GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_mla_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    entry = t.get(kernel)
+    if not entry or entry.get("source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock / throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        inside = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
+        note = None
+        if not inside:
+            inside = rows
+            note = "timed region shorter than the sampling interval: samples span the run"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3])
+                          if v.lower().startswith("active")})
+        out = {"sm_mhz": statistics.median(r[1] for r in inside),
+               "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+               "samples": len(inside)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# ----------------------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------------------
+
+def max_over_ranks(local_seconds: float, dist=None, device=None) -> float:
+    """The timed region's length as the max over ranks (the slowest replica sets the time)."""
+    if dist is None:
+        return local_seconds
+    import torch
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Units processed by all ranks (each runs its own replica) per second of the slowest."""
+    return units_per_rank * world / seconds
+
+
+def _device_problem(d, fp8=False):
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_util import DeviceDecompress
+    return DeviceDecompress(d, fp8=fp8)
+
+
+def _time_steps(step, steps, warmup, flush, stream, event_pairs=None):
+    """Runs warmup untimed steps, then `steps` timed ones with an L2 flush before each;
+    returns the summed device time (s) of the timed steps."""
+    import torch
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import workloads
+    import paged_kv_mla_gb300 as pkm
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    peaks, peak_kind = load_peaks()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", rank=rank, world_size=world, device_id=dev)
+
+    # ---------------- headline: DeepSeek-V3-shaped bf16 decompress ----------------
+    d = workloads.WORKLOADS["deepseek_v3_bf16_decompress"]()
+    g = _device_problem(d)
+    rows = min(int(d.buffer_row_offsets[-1]), d.buffer_length)
+    flop = d.flops
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    for _ in range(args.warmup):
+        g.run()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_dev = _time_steps(g.run, args.steps, 0, flush, stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    wall1 = time.time()
+    if sampler:
+        sampler.mark(wall0, wall1)
+    t_max = max_over_ranks(t_dev, dist, dev)
+    assert int(g.status.item()) == 0, "device status reported an error"
+    per_step = t_max / args.steps
+    value = whole_job_rate(flop * args.steps, world, t_max) / 1e12
+    achieved = flop / per_step / 1e12
+
+    if sampler:
+        time.sleep(0.25)
+        sampler.stop()
+    if rank != 0:
+        if dist:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    extra = {}
+    # ---------------- secondary rows (rank 0 only, fewer steps) ----------------
+    sec_steps = max(5, min(args.steps, 50))
+    d8 = workloads.WORKLOADS["deepseek_v3_fp8_decompress"]()
+    g8 = _device_problem(d8, fp8=True)
+    t8 = _time_steps(g8.run, sec_steps, 3, flush, stream) / sec_steps
+    assert int(g8.status.item()) == 0
+    b8 = 2 * (d8.buffer_length * (2 * d8.latent_cols + 2 * d8.n_out)) + d8.n_out * d8.kv_lora_rank
+    extra["fp8_decompress"] = {
+        "workload": d8.name, "rows": d8.buffer_length, "ms": t8 * 1e3,
+        "tflops": d8.flops / t8 / 1e12, "rows_per_s": d8.buffer_length / t8,
+        "hbm_gbs": b8 / t8 / 1e9, "hbm_frac_of_measured": b8 / t8 / 1e9 / peaks["hbm_gbs"],
+        "launches_per_step": 2}
+    del g8
+    dl = workloads.WORKLOADS["long_context_decompress"]()
+    gl = _device_problem(dl)
+    tl = _time_steps(gl.run, max(3, sec_steps // 4), 2, flush, stream) / max(3, sec_steps // 4)
+    assert int(gl.status.item()) == 0
+    extra["long_context_decompress"] = {
+        "workload": dl.name, "rows": dl.buffer_length, "ms": tl * 1e3,
+        "tflops": dl.flops / tl / 1e12, "rows_per_s": dl.buffer_length / tl,
+        "frac_of_measured_bf16": dl.flops / tl / 1e12 / peaks["bf16_tflops"]}
+    del gl
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_util import DeviceKvMatmul
+    km = workloads.WORKLOADS["kv_matmul_write_path"]()
+    gk = DeviceKvMatmul(km)
+    tk = _time_steps(gk.run, sec_steps, 3, flush, stream) / sec_steps
+    assert int(gk.status.item()) == 0
+    t_roof = max(km.flops / (peaks["bf16_tflops"] * 1e12), km.bytes_moved / (peaks["hbm_gbs"] * 1e9))
+    extra["kv_matmul"] = {
+        "workload": km.name, "rows": km.total_rows, "ms": tk * 1e3,
+        "tflops": km.flops / tk / 1e12, "gbs": km.bytes_moved / tk / 1e9,
+        "roofline_frac": t_roof / tk}
+    del gk
+
+    # ---------------- end to end: host buffers through the C ABI ----------------
+    e2e = run_e2e(d, max(3, min(args.steps, 10)))
+
+    # ---------------- CPU oracle on a bounded sample ----------------
+    cpu = cpu_baseline_sample(d, args.cpu_rows)
+
+    algo_bytes = rows * (2 * d.latent_cols * 2 + 2 * d.n_out) + d.n_out * d.kv_lora_rank * 2
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded)",
+        "config": {"workload": d.name, "batch": d.batch, "buffer_length": d.buffer_length,
+                   "kv_lora_rank": d.kv_lora_rank, "qk_rope_head_dim": d.rope_dim,
+                   "n_out": d.n_out, "page_size": d.page_size, "num_pages": d.num_pages,
+                   "l2": "flushed before every timed step (256 MiB write, untimed)",
+                   "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
+        "rows_per_s": whole_job_rate(rows * args.steps, world, t_max),
+        "pct_tensor_peak": 100.0 * achieved / peaks["bf16_tflops"],
+        "roofline": {"bound": "tensor", "kernel": "decompress_bf16_kernel",
+                     "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "peak_kind": peak_kind + " burst",
+                     "traffic": profiled_traffic("decompress_bf16_kernel"),
+                     "algorithmic_bytes": algo_bytes,
+                     "hbm_gbs_algorithmic": algo_bytes / per_step / 1e9},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": sampler.summary() if sampler else None,
+        "gpu_launches": args.steps,
+        "extra": extra,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(d, steps):
+    """TFLOP/s through the public call with the step's inputs in pinned host memory: H2D of
+    cache, page table, offsets and W_k, the decompress, D2H of k_latent_buffer and k_buffer,
+    all inside CUDA events on the stream."""
+    import numpy as np
+    import torch
+    from gpu_util import DeviceDecompress
+
+    g = DeviceDecompress(d)
+    host_in = [torch.from_numpy(np.ascontiguousarray(a).view(np.int16 if a.dtype == np.uint16 else np.int32)).pin_memory()
+               for a in (d.cache, d.page_table, d.buffer_row_offsets, d.cache_offsets, d.w_k)]
+    dev_in = [g.cache, g.pt, g.bro, g.co, g.w]
+    host_out = [torch.empty(g.k_latent.shape, dtype=torch.int16).pin_memory(),
+                torch.empty(g.k_buffer.shape, dtype=torch.int16).pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for h, dv in zip(host_in, dev_in):
+            dv.copy_(h, non_blocking=True)
+        g.run()
+        host_out[0].copy_(g.k_latent, non_blocking=True)
+        host_out[1].copy_(g.k_buffer, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    t = s.elapsed_time(e) / 1e3 / steps
+    return {"value": d.flops / t / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": t * 1e3}
+
+
+def cpu_baseline_sample(d, sample_rows):
+    """The oracle, as it stands (single thread), on the first `sample_rows` rows of the
+    workload: gather + fp64 triple loop.  Reported as TFLOP/s."""
+    import numpy as np
+    import oracle
+    from util import cache_view
+
+    n = min(sample_rows, d.buffer_length)
+    t0 = time.perf_counter()
+    st, lat, kb, written = oracle.decompress_k(cache_view(d), d.layer_idx, d.buffer_row_offsets,
+                                               d.cache_offsets, d.batch, n, d.kv_lora_rank,
+                                               d.rope_dim, d.w_k)
+    t = time.perf_counter() - t0
+    flop = 2 * int(written.sum()) * d.kv_lora_rank * d.n_out
+    return {"value": flop / t / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n} rows of {d.name} ({d.buffer_length} rows), whole rows "
+                      f"(gather + {d.n_out} fp64 dot products of {d.kv_lora_rank}); {t:.1f} s",
+            "seconds": t}
+
+
+# ----------------------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ----------------------------------------------------------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import workloads
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from util import cache_view
+
+    d = workloads.WORKLOADS["deepseek_v3_bf16_decompress"]()
+    rows_per_step = args.ref_rows
+    bro = d.buffer_row_offsets
+    # each step: a different window of rows, expressed as a sub-problem of the same workload
+    def step(i):
+        start = (i * rows_per_step) % max(1, d.buffer_length - rows_per_step)
+        sub_bro = bro.astype("int64").clip(start, start + rows_per_step) - start
+        sub_co = d.cache_offsets.astype("int64").copy()
+        for b in range(d.batch):
+            sub_co[b] += max(0, start - int(bro[b]))
+        st, lat, kb, written = oracle.decompress_k(
+            cache_view(d), d.layer_idx, sub_bro.astype("uint32"), sub_co.astype("uint32"),
+            d.batch, rows_per_step, d.kv_lora_rank, d.rope_dim, d.w_k)
+        return int(written.sum())
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    done = 0
+    for i in range(args.steps):
+        done += step(args.warmup + i)
+    t = time.perf_counter() - t0
+    flop = 2 * done * d.kv_lora_rank * d.n_out
+    value = flop / t / 1e12
+    sample = (f"{rows_per_step} consecutive rows of {d.name} per step (gather + "
+              f"{d.n_out} fp64 dot products of {d.kv_lora_rank} per row), single thread")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": d.name, "batch": d.batch, "buffer_length": d.buffer_length,
+                       "kv_lora_rank": d.kv_lora_rank, "qk_rope_head_dim": d.rope_dim,
+                       "n_out": d.n_out, "page_size": d.page_size},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=768,
+                    help="rows of the workload the CPU oracle baseline computes")
+    ap.add_argument("--ref-rows", type=int, default=16,
+                    help="rows per step of the reference (oracle) arm")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus > 1 and world == 1 and "RANK" not in os.environ:
+        ap.error("--gpus > 1 must be launched with torch.distributed.run (one rank per GPU)")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -201,6 +201,16 @@ pkm_status kv_matmul_paged(const void* hidden_state, const uint32_t* input_row_o
                            const void* weight, int32_t n_out, const pkm_paged_cache* kv_cache,
                            uint32_t layer_idx, int32_t* dev_status, void* stream);
 
+/*
+ * Failure-detection self check (no counterpart on the pages).  Launches one CTA that waits,
+ * with the same bounded mbarrier wait every kernel above uses, on a barrier phase that
+ * nothing completes.  After timeout_ms (1..5000) the wait gives up and PKM_ERR_TIMEOUT is
+ * merged into *dev_status (device int32, required); the kernel then returns normally and
+ * the CUDA context stays usable.  Returns PKM_ERR_INVALID_ARG for a NULL status or a limit
+ * out of range.
+ */
+pkm_status pkm_check_wait_timeout(int32_t* dev_status, uint32_t timeout_ms, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* pkm_status_string(pkm_status status);
 

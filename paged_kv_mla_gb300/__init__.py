@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(_HERE, "libpaged_kv_mla.so")
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"{LIB_PATH} is missing: build the CUDA library first "
-        "(python -m paged_kv_mla_gb300.build, or __graft_entry__.build()).")
+        "(python paged_kv_mla_gb300/build.py, or __graft_entry__.build()).")
 
 _lib = ctypes.CDLL(LIB_PATH)
 
@@ -67,6 +67,8 @@ _lib.mla_decompress_k_paged_fp8.restype = ctypes.c_int
 _lib.kv_matmul_paged.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _i32, ctypes.POINTER(_CCache),
                                  _u32, _vp, _vp]
 _lib.kv_matmul_paged.restype = ctypes.c_int
+_lib.pkm_check_wait_timeout.argtypes = [_vp, _u32, _vp]
+_lib.pkm_check_wait_timeout.restype = ctypes.c_int
 
 
 def status_string(code: int) -> str:
@@ -181,7 +183,13 @@ def kv_matmul_paged(hidden_state: torch.Tensor, input_row_offsets: torch.Tensor,
     return _check(code, "kv_matmul_paged", check)
 
 
-__all__ = ["PagedCache", "PkmError", "mla_decompress_k_paged", "mla_decompress_k_paged_fp8",
+def pkm_check_wait_timeout(dev_status: torch.Tensor, timeout_ms: int, stream=None,
+                           check: bool = True) -> int:
+    code = _lib.pkm_check_wait_timeout(_ptr(dev_status), int(timeout_ms), _stream(stream))
+    return _check(code, "pkm_check_wait_timeout", check)
+
+
+__all__ = ["pkm_check_wait_timeout", "PagedCache", "PkmError", "mla_decompress_k_paged", "mla_decompress_k_paged_fp8",
            "mla_decompress_k_paged_fp8_workspace_size", "fp8_workspace_views", "kv_matmul_paged",
            "status_string", "LIB_PATH", "PKM_OK", "PKM_ERR_INVALID_ARG", "PKM_ERR_UNSUPPORTED",
            "PKM_ERR_CUDA", "PKM_ERR_OUT_OF_RANGE", "PKM_ERR_TIMEOUT"]

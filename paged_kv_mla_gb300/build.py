@@ -2,8 +2,8 @@
 
 Each translation unit under csrc/ is compiled in parallel into _build/, then linked into a
 shared library next to this file (CUDA runtime linked statically, so the library depends
-only on the driver at run time).  Run ``python -m paged_kv_mla_gb300.build`` or call
-``build()``; ``__graft_entry__.build()`` does the same.
+only on the driver at run time).  Run ``python paged_kv_mla_gb300/build.py`` (as a script:
+importing the package needs the library this builds) or ``__graft_entry__.build()``.
 """
 from __future__ import annotations
 
@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpaged_kv_mla.so")
-SOURCES = ["api.cu", "decompress_bf16.cu", "decompress_fp8.cu", "kv_matmul.cu"]
+SOURCES = ["api.cu", "decompress_bf16.cu", "decompress_fp8.cu", "kv_matmul.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

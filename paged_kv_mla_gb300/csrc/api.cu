@@ -318,4 +318,12 @@ pkm_status kv_matmul_paged(const void* hidden_state, const uint32_t* input_row_o
                : PKM_ERR_CUDA;
 }
 
+pkm_status pkm_check_wait_timeout(int32_t* dev_status, uint32_t timeout_ms, void* stream) {
+    if (dev_status == nullptr || timeout_ms == 0 || timeout_ms > 5000) return PKM_ERR_INVALID_ARG;
+    return pkm::launch_wait_timeout_check(dev_status, static_cast<uint64_t>(timeout_ms) * 1000000ull,
+                                          static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKM_OK
+               : PKM_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -73,6 +73,7 @@ cudaError_t launch_decompress_fp8_gemm(const CUtensorMap& tm_q, const CUtensorMa
                                        Fp8Extra extra, int num_sms, cudaStream_t stream);
 cudaError_t launch_kv_matmul(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                              KvMatmulArgs args, int num_sms, cudaStream_t stream);
+cudaError_t launch_wait_timeout_check(int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 
 // Row bookkeeping shared by the decompress kernels: element offset (inside the layer) of
 // the cache slot that feeds output row r, -1 when no request covers r (or r >= row_end),

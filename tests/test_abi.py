@@ -14,9 +14,10 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lib():
-    from paged_kv_mla_gb300 import build
-    path = build.build()
-    return ctypes.CDLL(path)
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_mla_gb300
+    return ctypes.CDLL(paged_kv_mla_gb300.LIB_PATH)
 
 
 def declared_functions():

@@ -327,3 +327,14 @@ def test_empty_problems_launch_nothing():
     assert gk.run() == pkm.PKM_OK
     out, status = gk.results()
     assert status == 0 and np.array_equal(out, k.cache)
+
+
+def test_bounded_wait_times_out_and_context_stays_usable():
+    """Failure detection without a fault: a wait that nothing satisfies gives up after its
+    limit, reports PKM_ERR_TIMEOUT, and the next launch on the same context is correct."""
+    import paged_kv_mla_gb300 as pkm
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkm.pkm_check_wait_timeout(st, 200)
+    torch.cuda.synchronize()
+    assert int(st.item()) == pkm.PKM_ERR_TIMEOUT
+    check_full_decompress(workloads.tiny_decompress())
