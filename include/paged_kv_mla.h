@@ -174,6 +174,40 @@ pkm_status mla_decompress_k_paged_fp8(const pkm_paged_cache* cache, uint32_t lay
                                       void* stream);
 
 /*
+ * FP8 decompress for callers that cannot allocate device memory.  The paper has no
+ * counterpart: this entry point exists for users of this library, not for the method.
+ *
+ * Some callers cannot call cudaMalloc or an allocator of their own: a plug-in inside an
+ * engine that hands out only the buffers it planned up front, or a latency-critical serving
+ * loop where an allocation (which may synchronise the whole device) is not acceptable.
+ * This call computes exactly what mla_decompress_k_paged_fp8 computes, with the same
+ * arguments minus the workspace: the quantised latent goes to a fixed array of
+ * PKM_FP8_NOALLOC_SCRATCH_BYTES (16 MiB) that the library keeps in device memory.  Every
+ * GPU on which the library's device code is loaded holds that array until the process
+ * exits.  No call allocates or frees memory.
+ *
+ *   - Size limit: mla_decompress_k_paged_fp8_workspace_size(buffer_length, kv_lora_rank)
+ *     must not exceed PKM_FP8_NOALLOC_SCRATCH_BYTES (for kv_lora_rank 512: at most 31 775
+ *     rows); larger calls return PKM_ERR_UNSUPPORTED and launch nothing.
+ *   - Set-up: the first call on a device (with that device current) looks up the array's
+ *     device address and caches it; make that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same array and leaves its contents behind.
+ *     Nothing in it needs to start at zero.  Calls whose kernels overlap on the GPU (other
+ *     streams, other threads) race on the array: order them on one stream or serialise them.
+ *   - The quantised codes and scales are not returned; use mla_decompress_k_paged_fp8 with
+ *     your own workspace to read them.
+ */
+#define PKM_FP8_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+pkm_status mla_decompress_k_paged_fp8_noalloc(const pkm_paged_cache* cache, uint32_t layer_idx,
+                                              const uint32_t* buffer_row_offsets,
+                                              const uint32_t* cache_offsets, int32_t batch,
+                                              int32_t buffer_length, int32_t kv_lora_rank,
+                                              int32_t rope_dim, const void* w_k_e4m3,
+                                              const float* w_k_scale, int32_t n_out,
+                                              void* k_latent_buffer, void* k_buffer,
+                                              int32_t* dev_status, void* stream);
+
+/*
  * Ragged GEMM written into the paged K/V cache.
  * Source: kv_matmul_ragged_paged -- description ("performs a matmul, writing the output
  * into" the KV cache collection) and Args hidden_state (sum(seq_lens), num_heads *

@@ -67,6 +67,11 @@ _lib.mla_decompress_k_paged_fp8.restype = ctypes.c_int
 _lib.kv_matmul_paged.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _i32, ctypes.POINTER(_CCache),
                                  _u32, _vp, _vp]
 _lib.kv_matmul_paged.restype = ctypes.c_int
+_lib.mla_decompress_k_paged_fp8_noalloc.argtypes = [ctypes.POINTER(_CCache), _u32, _vp, _vp, _i32,
+                                                    _i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp,
+                                                    _vp, _vp]
+_lib.mla_decompress_k_paged_fp8_noalloc.restype = ctypes.c_int
+FP8_NOALLOC_SCRATCH_BYTES = 16 << 20
 _lib.pkm_check_wait_timeout.argtypes = [_vp, _u32, _vp]
 _lib.pkm_check_wait_timeout.restype = ctypes.c_int
 
@@ -170,6 +175,26 @@ def mla_decompress_k_paged_fp8(cache: PagedCache, layer_idx: int,
     return _check(code, "mla_decompress_k_paged_fp8", check)
 
 
+def mla_decompress_k_paged_fp8_noalloc(cache: PagedCache, layer_idx: int,
+                                       buffer_row_offsets: torch.Tensor,
+                                       cache_offsets: torch.Tensor, buffer_length: int,
+                                       kv_lora_rank: int, rope_dim: int, w_k_e4m3: torch.Tensor,
+                                       w_k_scale: torch.Tensor, k_latent_buffer: torch.Tensor,
+                                       k_buffer: torch.Tensor,
+                                       dev_status: Optional[torch.Tensor] = None, stream=None,
+                                       check: bool = True) -> int:
+    """The FP8 decompress without a caller workspace, for callers that cannot allocate
+    device memory: the library's fixed 16 MiB device array holds the quantised latent."""
+    c = cache.c_struct()
+    batch = int(buffer_row_offsets.shape[0]) - 1
+    code = _lib.mla_decompress_k_paged_fp8_noalloc(
+        ctypes.byref(c), int(layer_idx), _ptr(buffer_row_offsets), _ptr(cache_offsets), batch,
+        int(buffer_length), int(kv_lora_rank), int(rope_dim), _ptr(w_k_e4m3), _ptr(w_k_scale),
+        int(w_k_e4m3.shape[0]), _ptr(k_latent_buffer), _ptr(k_buffer), _ptr(dev_status),
+        _stream(stream))
+    return _check(code, "mla_decompress_k_paged_fp8_noalloc", check)
+
+
 def kv_matmul_paged(hidden_state: torch.Tensor, input_row_offsets: torch.Tensor,
                     weight: torch.Tensor, kv_cache: PagedCache, layer_idx: int,
                     dev_status: Optional[torch.Tensor] = None, stream=None,
@@ -189,7 +214,8 @@ def pkm_check_wait_timeout(dev_status: torch.Tensor, timeout_ms: int, stream=Non
     return _check(code, "pkm_check_wait_timeout", check)
 
 
-__all__ = ["pkm_check_wait_timeout", "PagedCache", "PkmError", "mla_decompress_k_paged", "mla_decompress_k_paged_fp8",
+__all__ = ["pkm_check_wait_timeout", "mla_decompress_k_paged_fp8_noalloc",
+           "FP8_NOALLOC_SCRATCH_BYTES", "PagedCache", "PkmError", "mla_decompress_k_paged", "mla_decompress_k_paged_fp8",
            "mla_decompress_k_paged_fp8_workspace_size", "fp8_workspace_views", "kv_matmul_paged",
            "status_string", "LIB_PATH", "PKM_OK", "PKM_ERR_INVALID_ARG", "PKM_ERR_UNSUPPORTED",
            "PKM_ERR_CUDA", "PKM_ERR_OUT_OF_RANGE", "PKM_ERR_TIMEOUT"]

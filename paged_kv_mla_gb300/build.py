@@ -18,7 +18,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpaged_kv_mla.so")
-SOURCES = ["api.cu", "decompress_bf16.cu", "decompress_fp8.cu", "kv_matmul.cu", "selftest.cu"]
+SOURCES = ["api.cu", "decompress_bf16.cu", "decompress_fp8.cu", "kv_matmul.cu", "selftest.cu",
+           "decompress_fp8_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
