@@ -45,25 +45,35 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {
+    "decompress_bf16_kernel": ["decompress_bf16.cu"],
+    "decompress_fp8_gemm_kernel": ["decompress_fp8.cu"],
+    "fp8_gather_quantize_kernel": ["decompress_fp8.cu"],
+    "kv_matmul_kernel": ["kv_matmul.cu"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources a kernel is built from (its .cu file plus the shared headers)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_mla_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = KERNEL_SOURCES[kernel] + ["pkm_device.cuh", "pkm_internal.h"]
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
-    kernel sources (else None)."""
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json), if it
+    was taken on the kernel's current sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         t = json.load(f)
     entry = t.get(kernel)
-    if not entry or entry.get("source_hash") != kernel_source_hash():
+    if not entry or entry.get("source_hash") != kernel_source_hash(kernel):
         return None
     return entry.get("dram_bytes_per_launch")
 

@@ -191,9 +191,12 @@ pkm_status mla_decompress_k_paged(const pkm_paged_cache* cache, uint32_t layer_i
                                             k_latent_buffer, k_buffer, dev_status, bn);
     int sms = 0;
     if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
+    // CTA-pair tiles: 256 rows (128 per CTA) x bn columns; each CTA loads bn/2 W_k rows
+    a.m_tiles = (buffer_length + 255) / 256;
+    a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
     alignas(64) CUtensorMap tm_w, tm_k;
     if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_k, kv_lora_rank, n_out,
-                   static_cast<uint64_t>(kv_lora_rank) * 2, 64, bn) ||
+                   static_cast<uint64_t>(kv_lora_rank) * 2, 64, bn / 2) ||
         !encode_2d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_buffer, n_out, buffer_length,
                    static_cast<uint64_t>(n_out) * 2, 64, 32))
         return PKM_ERR_CUDA;

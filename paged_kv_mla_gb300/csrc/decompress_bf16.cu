@@ -1,4 +1,4 @@
-// decompress_bf16.cu -- fused paged gather + tcgen05 up-projection (bf16).
+// decompress_bf16.cu -- fused paged gather + tcgen05 up-projection (bf16), on CTA pairs.
 //
 // generic_flare_mla_decompress_k_cache_ragged_paged (Modular MAX, nn/kv_cache_ragged),
 // description and Args: rows [buffer_row_offsets[b], buffer_row_offsets[b+1]) of the
@@ -6,19 +6,25 @@
 // they are copied to k_latent_buffer and their first kv_lora_rank columns are multiplied
 // by W_k^T into k_buffer.
 //
-// One persistent CTA per SM walks a contiguous range of 128 x bn output tiles (tile id =
-// m_tile * n_tiles + n_tile, so a CTA revisits the same 128 latent rows for consecutive
-// n tiles and gathers them once per range segment).  Warp roles:
-//   warp 0      TMA producer: W_k tiles [bn x 64] (128-byte swizzle) into a 2-stage ring.
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (M=128, N=bn, K=16).
-//   warps 2-3   gatherers: resolve each row through buffer_row_offsets / cache_offsets /
-//               the page table, cp.async the row's nope columns straight into the
-//               swizzled A tile (one cp.async group per 64-column k-block, each signalled
-//               on its own mbarrier), and copy the full latent row to k_latent_buffer.
-//   warps 4-7   epilogue: tcgen05.ld the fp32 accumulator (TMEM double-buffered), round to
-//               bf16, stage in swizzled shared memory, TMA-store 32 x 64 boxes of k_buffer.
-// The A tile (128 rows x kv_lora_rank) stays resident in shared memory for every n tile
-// of its segment; the MMA of a tile overlaps the epilogue of the previous one.
+// The grid is made of clusters of two CTAs on two SMs (a CTA pair).  A pair computes
+// 256 x bn output tiles with tcgen05.mma.cta_group::2 (M = 256): each CTA gathers and keeps
+// its own 128 latent rows (A) in shared memory and loads one half (bn/2 rows) of each W_k
+// tile (B); the even CTA issues the MMAs, which read both CTAs' shared memory and write
+// each CTA's 128 x bn accumulator into its own TMEM.  Splitting B halves the W_k bytes each
+// SM pulls from L2 per FLOP and halves the shared memory one pipeline stage needs, so each
+// CTA keeps four W_k stages in flight next to its resident A tile.
+//
+// Each pair walks a contiguous range of tile ids (m_pair * n_tiles + n), so consecutive
+// tiles reuse the gathered rows.  Warp roles, in both CTAs:
+//   warp 0      TMA producer: this CTA's half of W_k [bn/2 x 64] (128-byte swizzle) into a
+//               4-stage ring; completion is signalled on the even CTA's barrier.
+//   warp 1      TMEM allocator (pair); in the even CTA also the single MMA-issuing thread.
+//   warps 2-3   gatherers: resolve rows through buffer_row_offsets / cache_offsets / the
+//               page table, cp.async the nope columns into the swizzled A tile (one group
+//               and one barrier arrival per 64-column k-block), copy whole latent rows to
+//               k_latent_buffer.
+//   warps 4-7   epilogue: tcgen05.ld of this CTA's accumulator (double-buffered), bf16
+//               rounding, swizzled staging, TMA stores of 32 x 64 boxes of k_buffer.
 #include "pkm_device.cuh"
 #include "pkm_internal.h"
 
@@ -26,23 +32,23 @@ namespace pkm {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBM = 128;
+constexpr int kBM = 128;                     // rows per CTA (256 per pair)
 constexpr int kKBMax = 8;                    // kv_lora_rank <= 512 = 8 k-blocks of 64
 constexpr int kABlockBytes = kBM * 128;      // 16 KB per k-block
-constexpr int kStages = 2;
-constexpr int kBStageBytes = 256 * 128;      // bn <= 256 rows of 128 bytes
+constexpr int kStages = 4;
+constexpr int kBStageBytes = 128 * 128;      // bn/2 <= 128 rows of 128 bytes
 constexpr int kEpiWarps = 4;
 constexpr int kOutBufBytes = 32 * 128;       // 32 rows x 64 bf16
 constexpr int kGatherThreads = 64;
 constexpr uint32_t kTmemCols = 512;
 
 struct Bars {
-    uint64_t b_full[kStages];
-    uint64_t b_empty[kStages];
-    uint64_t a_full[kKBMax];
-    uint64_t a_empty;
-    uint64_t t_full[2];
-    uint64_t t_empty[2];
+    uint64_t b_full[kStages];   // even CTA: both halves of a W_k stage landed
+    uint64_t b_empty[kStages];  // both CTAs: the pair's MMAs are done with a stage
+    uint64_t a_full[kKBMax];    // even CTA: k-block of both CTAs' A gathered
+    uint64_t a_empty;           // both CTAs: the MMAs are done with A
+    uint64_t t_full[2];         // both CTAs: accumulator ready
+    uint64_t t_empty[2];        // even CTA: both CTAs' epilogues drained an accumulator
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -57,7 +63,7 @@ constexpr size_t kOffBars = kOffRows + kBM * sizeof(int64_t);
 constexpr size_t kSmemBytes = kOffBars + sizeof(Bars) + 1024;  // + base alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decompress_bf16_kernel(const __grid_constant__ CUtensorMap tm_w,
                            const __grid_constant__ CUtensorMap tm_kbuf, const DecompressArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -71,23 +77,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0 = even CTA (issues the MMAs), 1 = odd
+    const bool leader = rank == 0;
     const int KB = a.kv_lora_rank / 64;
-    const int bn = a.bn;
-    const int64_t T = a.total_tiles;
-    const int64_t G = gridDim.x;
-    const int64_t t_begin = T * blockIdx.x / G;
-    const int64_t t_end = T * (blockIdx.x + 1) / G;
+    const int bn = a.bn;                      // pair N tile
+    const int half = bn / 2;                  // W_k rows this CTA loads per tile
+    const int64_t T = a.total_tiles;          // pair tiles
+    const int64_t P = gridDim.x / 2;
+    const int64_t pair = blockIdx.x / 2;
+    const int64_t t_begin = T * pair / P;
+    const int64_t t_end = T * (pair + 1) / P;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars->b_full[s], 1);
             mbar_init(&bars->b_empty[s], 1);
         }
-        for (int kb = 0; kb < kKBMax; ++kb) mbar_init(&bars->a_full[kb], kGatherThreads);
+        for (int kb = 0; kb < kKBMax; ++kb) mbar_init(&bars->a_full[kb], 2 * kGatherThreads);
         mbar_init(&bars->a_empty, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->t_full[i], 1);
-            mbar_init(&bars->t_empty[i], kEpiWarps);
+            mbar_init(&bars->t_empty[i], 2 * kEpiWarps);
         }
         mbar_init(&bars->mma_done, 1);
         bars->abort_flag = 0;
@@ -95,8 +105,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(&bars->tmem_base, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(&bars->tmem_base, kTmemCols);
+        tmem_relinquish_pair();
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tm_w);
@@ -104,44 +114,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();  // the peer's barriers are initialised before any remote signal
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const WaitCtl wc{&bars->abort_flag, a.status, a.timeout_ns};
     const int64_t row_end = decompress_row_end(a);
 
     if (warp == 0) {
-        // ---------------- W_k producer ----------------
+        // ---------------- W_k producer (this CTA's half of each tile) ----------------
         if (lane == 0) {
             const uint64_t keep = policy_evict_last();
             uint32_t it = 0;
-            bool issued[kStages] = {false, false};
-            uint32_t last_phase[kStages] = {0, 0};
+            bool issued[kStages] = {};
+            uint32_t last_phase[kStages] = {};
             bool ok = true;
             for (int64_t t = t_begin; t < t_end && ok; ++t) {
                 const int n = static_cast<int>(t % a.n_tiles);
                 for (int kb = 0; kb < KB; ++kb) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1;
-                    if (!mbar_wait(&bars->b_empty[s], ph ^ 1, wc)) {
+                    if (!mbar_wait_cluster(&bars->b_empty[s], ph ^ 1, wc)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&bars->b_full[s], static_cast<uint32_t>(bn) * 128);
-                    tma_load_2d_hint(sB + s * kBStageBytes, &tm_w, &bars->b_full[s], kb * 64,
-                                     n * bn, keep);
+                    if (leader)  // both halves complete on the even CTA's barrier
+                        mbar_arrive_expect_tx(&bars->b_full[s], static_cast<uint32_t>(bn) * 128);
+                    tma_load_2d_pair(sB + s * kBStageBytes, &tm_w,
+                                     mapa_shared(smem_u32(&bars->b_full[s]), 0), kb * 64,
+                                     n * bn + static_cast<int>(rank) * half, keep);
                     issued[s] = true;
                     last_phase[s] = ph;
                     ++it;
                 }
             }
             if (!ok) {  // let loads already in flight land before the CTA retires
-                for (int s = 0; s < kStages; ++s)
-                    if (issued[s]) mbar_wait(&bars->b_full[s], last_phase[s], wc, false);
+                if (leader) {
+                    for (int s = 0; s < kStages; ++s)
+                        if (issued[s]) mbar_wait_cluster(&bars->b_full[s], last_phase[s], wc, false);
+                } else {
+                    spin_ns(50000);
+                }
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(128, bn, false, false);
+        // ---------------- MMA issuer (even CTA) ----------------
+        if (leader && lane == 0) {
+            const uint32_t idesc = idesc_bf16(256, bn, false, false);
             uint32_t it = 0, tile_i = 0, seg = 0;
             int64_t cur_m = -1;
             bool ok = true;
@@ -150,22 +167,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool new_seg = (m != cur_m);
                 if (new_seg) {
                     if (cur_m >= 0) {
-                        mma_commit(&bars->a_empty);  // sA free once these MMAs retire
+                        mma_commit_pair(&bars->a_empty, 3);  // both A tiles free once retired
                         ++seg;
                     }
                     cur_m = m;
                 }
                 const uint32_t acc = tile_i & 1, aph = (tile_i >> 1) & 1;
-                if (!mbar_wait(&bars->t_empty[acc], aph ^ 1, wc)) break;
+                if (!mbar_wait_cluster(&bars->t_empty[acc], aph ^ 1, wc)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + acc * static_cast<uint32_t>(bn);
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (new_seg && !mbar_wait(&bars->a_full[kb], seg & 1, wc)) {
+                    if (new_seg && !mbar_wait_cluster(&bars->a_full[kb], seg & 1, wc)) {
                         ok = false;
                         break;
                     }
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1;
-                    if (!mbar_wait(&bars->b_full[s], ph, wc)) {
+                    if (!mbar_wait_cluster(&bars->b_full[s], ph, wc)) {
                         ok = false;
                         break;
                     }
@@ -174,21 +191,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t b_addr = smem_u32(sB + s * kBStageBytes);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_bf16(d, sdesc_sw128(a_addr + k * 32, 16, 1024),
-                                 sdesc_sw128(b_addr + k * 32, 16, 1024), idesc,
-                                 (kb | k) != 0 ? 1u : 0u);
-                    mma_commit(&bars->b_empty[s]);
+                        mma_bf16_pair(d, sdesc_sw128(a_addr + k * 32, 16, 1024),
+                                      sdesc_sw128(b_addr + k * 32, 16, 1024), idesc,
+                                      (kb | k) != 0 ? 1u : 0u);
+                    mma_commit_pair(&bars->b_empty[s], 3);
                     ++it;
                 }
                 if (!ok) break;
-                mma_commit(&bars->t_full[acc]);
+                mma_commit_pair(&bars->t_full[acc], 3);
                 ++tile_i;
             }
-            mma_commit(&bars->mma_done);
-            mbar_wait(&bars->mma_done, 0, wc, false);
+            mma_commit_pair(&bars->mma_done, 1);
+            mbar_wait_cluster(&bars->mma_done, 0, wc, false);
         }
     } else if (warp < 4) {
-        // ---------------- gatherers ----------------
+        // ---------------- gatherers (this CTA's 128 rows) ----------------
         const int g = threadIdx.x - 64;
         const int chunk = g & 7;   // 16-byte chunk inside a 128-byte k-block row
         const int rsub = g >> 3;   // row phase 0..7
@@ -196,10 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t seg = 0;
         int64_t cur_m = -1;
         for (int64_t t = t_begin; t < t_end; ++t) {
-            const int64_t m = t / a.n_tiles;
-            if (m == cur_m) continue;
-            cur_m = m;
-            const bool writer = (t % a.n_tiles) == 0;  // this CTA owns tile (m, 0)
+            const int64_t m_pair = t / a.n_tiles;
+            if (m_pair == cur_m) continue;
+            cur_m = m_pair;
+            const int64_t m = m_pair * 2 + rank;          // this CTA's 128-row block
+            const bool writer = (t % a.n_tiles) == 0;      // this pair owns tile (m_pair, 0)
             for (int i = g; i < kBM; i += kGatherThreads) {
                 const int64_t off = decompress_row_source(a, m * kBM + i, row_end);
                 if (off == -2) report(a.status, PKM_ERR_OUT_OF_RANGE);
@@ -207,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (g == 0)
                 bars->gather_go =
-                    (seg == 0 || mbar_wait(&bars->a_empty, (seg - 1) & 1, wc)) ? 1 : 0;
+                    (seg == 0 || mbar_wait_cluster(&bars->a_empty, (seg - 1) & 1, wc)) ? 1 : 0;
             named_bar_sync(1, kGatherThreads);
             if (!bars->gather_go) break;
             for (int kb = 0; kb < KB; ++kb) {
@@ -226,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = 0; kb < KB; ++kb) {
                 cp_async_wait_dyn(KB - 1 - kb);
                 fence_proxy_async_smem();
-                mbar_arrive(&bars->a_full[kb]);
+                mbar_arrive_cluster(mapa_shared(smem_u32(&bars->a_full[kb]), 0));
             }
             if (writer) {
                 const int total = kBM * cchunks;
@@ -257,22 +275,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cp_async_wait<0>();
     } else {
-        // ---------------- epilogue ----------------
-        const int q = warp & 3;  // TMEM lane quarter == 32-row slab of the tile
+        // ---------------- epilogue (this CTA's 128 rows) ----------------
+        const int q = warp & 3;  // TMEM lane quarter == 32-row slab of the CTA's rows
+        const uint32_t t_empty_leader = mapa_shared(smem_u32(&bars->t_empty[0]), 0);
         uint32_t tile_i = 0, st_i = 0;
-        int64_t cur_m = -1, my_row = 0;
+        int64_t cur_m = -1, my_row = 0, m = 0;
         bool slab_full = false, my_valid = false;
         for (int64_t t = t_begin; t < t_end; ++t) {
-            const int64_t m = t / a.n_tiles;
+            const int64_t m_pair = t / a.n_tiles;
             const int n = static_cast<int>(t % a.n_tiles);
-            if (m != cur_m) {
-                cur_m = m;
+            if (m_pair != cur_m) {
+                cur_m = m_pair;
+                m = m_pair * 2 + rank;
                 my_row = m * kBM + q * 32 + lane;
                 my_valid = decompress_row_source(a, my_row, row_end) >= 0;
                 slab_full = __all_sync(0xffffffffu, my_valid);
             }
             const uint32_t acc = tile_i & 1, ph = (tile_i >> 1) & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars->t_full[acc], ph, wc))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&bars->t_full[acc], ph, wc))) break;
             tc_fence_after();
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(bn);
@@ -315,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->t_empty[acc]);
+            if (lane == 0) mbar_arrive_cluster(t_empty_leader + acc * sizeof(uint64_t));
             ++tile_i;
         }
         if (lane == 0) bulk_wait<0>();
@@ -324,8 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();  // no CTA of the pair retires while the other may still signal it
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -336,8 +357,9 @@ cudaError_t launch_decompress_bf16(const CUtensorMap& tm_w, const CUtensorMap& t
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    const int64_t grid = args.total_tiles < num_sms ? args.total_tiles : num_sms;
-    decompress_bf16_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
+    const int64_t max_pairs = num_sms / 2;
+    const int64_t pairs = args.total_tiles < max_pairs ? args.total_tiles : max_pairs;
+    decompress_bf16_kernel<<<static_cast<unsigned>(2 * pairs), kThreads, kSmemBytes, stream>>>(
         tm_w, tm_kbuf, args);
     return cudaGetLastError();
 }

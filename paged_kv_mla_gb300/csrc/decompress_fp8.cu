@@ -14,7 +14,7 @@
 //      row is quantised exactly once, however many n tiles later consume it.
 //   2. decompress_fp8_gemm_kernel: persistent CTAs over 128 x 128 output tiles (one n
 //      tile = one weight-scale block).  TMA brings the quantised A tile (resident for the
-//      CTA's range segment) and W_k blocks of 128 x 128 e4m3 through a 6-stage ring;
+//      CTA's range segment) and W_k blocks of 128 x 128 e4m3 through an 8-stage ring;
 //      tcgen05.mma kind::f8f6f4 accumulates each 128-wide k-block into its own TMEM
 //      accumulator (4 x 128 columns), and the epilogue combines them in registers as
 //      sum_kb (s_a[row, kb] * s_w[n_tile, kb]) * acc_kb before rounding to bf16 and
@@ -99,7 +99,7 @@ constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kKBMax = 4;                     // kv_lora_rank <= 512
 constexpr int kABlockBytes = kBM * 128;       // 128 rows x 128 e4m3
-constexpr int kStages = 6;
+constexpr int kStages = 8;
 constexpr int kBStageBytes = kBN * 128;
 constexpr int kEpiWarps = 4;
 constexpr int kOutBufBytes = 32 * 128;

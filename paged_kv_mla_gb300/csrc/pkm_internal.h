@@ -32,7 +32,7 @@ struct DecompressArgs {
     // tiling, filled by the launcher
     int32_t bn;                    // N tile
     int32_t n_tiles;               // N / bn
-    int32_t m_tiles;               // ceil(L / 128)
+    int32_t m_tiles;               // ceil(L / rows per tile)
     int64_t total_tiles;           // m_tiles * n_tiles
 };
 
