@@ -303,9 +303,11 @@ pkm_status kv_matmul_paged(const void* hidden_state, const uint32_t* input_row_o
     a.cache_lengths = kv_cache->cache_lengths;
     a.status = dev_status;
     a.timeout_ns = wait_timeout_ns();
-    a.bn = pick_bn(n_out);
-    a.n_tiles = n_out / a.bn;
-    a.m_tiles = (total_rows + 127) / 128;
+    // CTA-pair tiles: 256 rows (128 per CTA) x bn columns, bn = 256 or 128; when n_out is an
+    // odd multiple of 64 the last 128-wide tile is half padding
+    a.bn = (n_out % 256 == 0) ? 256 : 128;
+    a.n_tiles = (n_out + a.bn - 1) / a.bn;
+    a.m_tiles = (total_rows + 255) / 256;
     a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
     int sms = 0;
     if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;

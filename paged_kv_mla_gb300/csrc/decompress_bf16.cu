@@ -12,19 +12,20 @@
 // tile (B); the even CTA issues the MMAs, which read both CTAs' shared memory and write
 // each CTA's 128 x bn accumulator into its own TMEM.  Splitting B halves the W_k bytes each
 // SM pulls from L2 per FLOP and halves the shared memory one pipeline stage needs, so each
-// CTA keeps four W_k stages in flight next to its resident A tile.
+// CTA keeps five W_k stages in flight next to its resident A tile.
 //
 // Each pair walks a contiguous range of tile ids (m_pair * n_tiles + n), so consecutive
 // tiles reuse the gathered rows.  Warp roles, in both CTAs:
 //   warp 0      TMA producer: this CTA's half of W_k [bn/2 x 64] (128-byte swizzle) into a
-//               4-stage ring; completion is signalled on the even CTA's barrier.
+//               5-stage ring; completion is signalled on the even CTA's barrier.
 //   warp 1      TMEM allocator (pair); in the even CTA also the single MMA-issuing thread.
 //   warps 2-3   gatherers: resolve rows through buffer_row_offsets / cache_offsets / the
 //               page table, cp.async the nope columns into the swizzled A tile (one group
 //               and one barrier arrival per 64-column k-block), copy whole latent rows to
 //               k_latent_buffer.
 //   warps 4-7   epilogue: tcgen05.ld of this CTA's accumulator (double-buffered), bf16
-//               rounding, swizzled staging, TMA stores of 32 x 64 boxes of k_buffer.
+//               rounding, a swizzled 4 KB staging box per warp, TMA stores of 32 x 64
+//               boxes of k_buffer.
 #include "pkm_device.cuh"
 #include "pkm_internal.h"
 
@@ -35,7 +36,7 @@ constexpr int kThreads = 256;
 constexpr int kBM = 128;                     // rows per CTA (256 per pair)
 constexpr int kKBMax = 8;                    // kv_lora_rank <= 512 = 8 k-blocks of 64
 constexpr int kABlockBytes = kBM * 128;      // 16 KB per k-block
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kBStageBytes = 128 * 128;      // bn/2 <= 128 rows of 128 bytes
 constexpr int kEpiWarps = 4;
 constexpr int kOutBufBytes = 32 * 128;       // 32 rows x 64 bf16
@@ -58,7 +59,7 @@ struct Bars {
 constexpr size_t kOffA = 0;
 constexpr size_t kOffB = kOffA + size_t(kKBMax) * kABlockBytes;
 constexpr size_t kOffOut = kOffB + size_t(kStages) * kBStageBytes;
-constexpr size_t kOffRows = kOffOut + size_t(kEpiWarps) * 2 * kOutBufBytes;
+constexpr size_t kOffRows = kOffOut + size_t(kEpiWarps) * kOutBufBytes;
 constexpr size_t kOffBars = kOffRows + kBM * sizeof(int64_t);
 constexpr size_t kSmemBytes = kOffBars + sizeof(Bars) + 1024;  // + base alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
@@ -278,7 +279,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---------------- epilogue (this CTA's 128 rows) ----------------
         const int q = warp & 3;  // TMEM lane quarter == 32-row slab of the CTA's rows
         const uint32_t t_empty_leader = mapa_shared(smem_u32(&bars->t_empty[0]), 0);
-        uint32_t tile_i = 0, st_i = 0;
+        uint32_t tile_i = 0;
         int64_t cur_m = -1, my_row = 0, m = 0;
         bool slab_full = false, my_valid = false;
         for (int64_t t = t_begin; t < t_end; ++t) {
@@ -309,8 +310,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
                 }
                 if (slab_full) {
-                    uint8_t* stage = sOut + (q * 2 + (st_i & 1)) * kOutBufBytes;
-                    if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer
+                    uint8_t* stage = sOut + q * kOutBufBytes;
+                    if (lane == 0) bulk_wait_read<0>();  // the previous store read its box
                     __syncwarp();
                     const uint32_t rowaddr = smem_u32(stage) + lane * 128;
 #pragma unroll
@@ -324,7 +325,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                      static_cast<int32_t>(m * kBM + q * 32));
                         bulk_commit();
                     }
-                    ++st_i;
                 } else if (my_valid) {  // slab with uncovered rows: plain per-row stores
                     uint16_t* dst = a.k_buffer + my_row * a.n_out + n * bn + c * 64;
 #pragma unroll

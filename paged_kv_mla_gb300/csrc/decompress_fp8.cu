@@ -16,7 +16,7 @@
 //      tile = one weight-scale block).  TMA brings the quantised A tile (resident for the
 //      CTA's range segment) and W_k blocks of 128 x 128 e4m3 through an 8-stage ring;
 //      tcgen05.mma kind::f8f6f4 accumulates each 128-wide k-block into its own TMEM
-//      accumulator (4 x 128 columns), and the epilogue combines them in registers as
+//      accumulator (4 x 128 columns), and 8 epilogue warps combine them in registers as
 //      sum_kb (s_a[row, kb] * s_w[n_tile, kb]) * acc_kb before rounding to bf16 and
 //      TMA-storing k_buffer.  An accumulator is released as soon as the epilogue has read
 //      it, so the next tile's MMAs overlap the rest of the epilogue.
@@ -94,14 +94,14 @@ __global__ void __launch_bounds__(256)
 // 2. block-scaled GEMM
 // ------------------------------------------------------------------------------------
 
-constexpr int kThreads = 192;                 // producer, MMA, 4 epilogue warps
+constexpr int kThreads = 320;                 // producer, MMA, 8 epilogue warps
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kKBMax = 4;                     // kv_lora_rank <= 512
 constexpr int kABlockBytes = kBM * 128;       // 128 rows x 128 e4m3
 constexpr int kStages = 8;
 constexpr int kBStageBytes = kBN * 128;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;
 constexpr int kOutBufBytes = 32 * 128;
 constexpr uint32_t kTmemCols = 512;           // kKBMax accumulators x 128 columns
 
@@ -120,7 +120,7 @@ struct Bars {
 constexpr size_t kOffA = 0;
 constexpr size_t kOffB = kOffA + size_t(kKBMax) * kABlockBytes;
 constexpr size_t kOffOut = kOffB + size_t(kStages) * kBStageBytes;
-constexpr size_t kOffBars = kOffOut + size_t(kEpiWarps) * 2 * kOutBufBytes;
+constexpr size_t kOffBars = kOffOut + size_t(kEpiWarps) * kOutBufBytes;
 constexpr size_t kSmemBytes = kOffBars + sizeof(Bars) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
 
@@ -265,8 +265,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&bars->mma_done, 0, wc, false);
         }
     } else {
+        // 8 epilogue warps: warp w reads TMEM lane quarter w % 4 (32 rows) and one 64-column
+        // half of the 128-column tile, so each keeps 64 fp32 partial sums and issues both
+        // 32-column TMEM loads of a k-block before waiting once.
         const int q = warp & 3;
-        uint32_t tile_i = 0, st_i = 0;
+        const int h = (warp - 2) >> 2;
+        uint8_t* stage = sOut + (warp - 2) * kOutBufBytes;
+        uint32_t tile_i = 0;
         int64_t cur_m = -1, my_row = 0;
         bool slab_full = false, my_valid = false;
         float sa[kKBMax] = {0.f, 0.f, 0.f, 0.f};
@@ -283,9 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < kKBMax; ++kb)
                     sa[kb] = (my_valid && kb < KB) ? x.q_scale[my_row * KB + kb] : 0.0f;
             }
-            float acc[kBN];
+            float acc[64];
 #pragma unroll
-            for (int j = 0; j < kBN; ++j) acc[j] = 0.0f;
+            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
 #pragma unroll
             for (int kb = 0; kb < kKBMax; ++kb) {
                 if (kb >= KB) break;
@@ -295,52 +300,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const float cs = sa[kb] * __ldg(x.w_scale + static_cast<int64_t>(n) * KB + kb);
-                const uint32_t tbase =
-                    tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(kb) * kBN;
-#pragma unroll
-                for (int p = 0; p < kBN / 32; ++p) {
-                    uint32_t v[32];
-                    tmem_ld_x32(tbase + p * 32, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        acc[p * 32 + j] = fmaf(cs, __uint_as_float(v[j]), acc[p * 32 + j]);
-                }
+                const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(kb) * kBN + h * 64;
+                uint32_t v0[32], v1[32];
+                tmem_ld_x32(tbase, v0);
+                tmem_ld_x32(tbase + 32, v1);
+                tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->t_empty[kb]);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    acc[j] = fmaf(cs, __uint_as_float(v0[j]), acc[j]);
+                    acc[32 + j] = fmaf(cs, __uint_as_float(v1[j]), acc[32 + j]);
+                }
             }
             if (!ok) break;
+            uint32_t p[32];
 #pragma unroll
-            for (int c = 0; c < kBN / 64; ++c) {
-                uint32_t p[32];
+            for (int j = 0; j < 32; ++j) p[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
+            const int col = n * kBN + h * 64;
+            if (slab_full) {
+                if (lane == 0) bulk_wait_read<0>();  // the previous store read this box
+                __syncwarp();
+                const uint32_t rowaddr = smem_u32(stage) + lane * 128;
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    p[j] = pack_bf16x2(acc[c * 64 + 2 * j], acc[c * 64 + 2 * j + 1]);
-                if (slab_full) {
-                    uint8_t* stage = sOut + (q * 2 + (st_i & 1)) * kOutBufBytes;
-                    if (lane == 0) bulk_wait_read<1>();
-                    __syncwarp();
-                    const uint32_t rowaddr = smem_u32(stage) + lane * 128;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        st_shared_v4(rowaddr + ((j ^ (lane & 7)) << 4), p[4 * j], p[4 * j + 1],
-                                     p[4 * j + 2], p[4 * j + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tm_kbuf, stage, n * kBN + c * 64,
-                                     static_cast<int32_t>(m * kBM + q * 32));
-                        bulk_commit();
-                    }
-                    ++st_i;
-                } else if (my_valid) {
-                    uint16_t* dst = a.k_buffer + my_row * a.n_out + n * kBN + c * 64;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        st_v4(dst + j * 8,
-                              make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(rowaddr + ((j ^ (lane & 7)) << 4), p[4 * j], p[4 * j + 1],
+                                 p[4 * j + 2], p[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tm_kbuf, stage, col, static_cast<int32_t>(m * kBM + q * 32));
+                    bulk_commit();
                 }
+            } else if (my_valid) {
+                uint16_t* dst = a.k_buffer + my_row * a.n_out + col;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_v4(dst + j * 8, make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));
             }
             ++tile_i;
         }

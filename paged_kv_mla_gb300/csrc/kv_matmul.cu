@@ -1,4 +1,4 @@
-// kv_matmul.cu -- ragged GEMM written into the paged K/V cache.
+// kv_matmul.cu -- ragged GEMM written into the paged K/V cache, on CTA pairs.
 //
 // kv_matmul_ragged_paged (Modular MAX, nn/kv_cache_ragged), description and Args: Y =
 // hidden_state [sum(seq_lens), num_heads*head_size] x weight [num_heads*head_size,
@@ -6,12 +6,15 @@
 // layer_idx at position cache_lengths[b] + i.  The output columns are split K then V
 // (head_elems each).
 //
-// Persistent CTAs over 128 x bn tiles.  Warp 0 streams A (hidden_state, K-major, box
-// 64 x 128) and B (weight, N contiguous = MN-major, bn/64 boxes of 64 x 64) with TMA into
-// a 4-stage ring; warp 1 issues tcgen05.mma (B described as MN-major, 128-byte swizzle);
-// warps 2-5 drain the double-buffered TMEM accumulator, round to bf16, and scatter each
-// row's 64-column chunk to its (page, slot) with 16-byte stores, 4 full rows of 128 bytes
-// per warp instruction.
+// Clusters of two CTAs compute 256 x bn tiles with tcgen05.mma.cta_group::2 (M = 256):
+// each CTA streams its own 128 rows of A (hidden_state, K-major, box 64 x 128) and half of
+// the tile's B columns (weight, N contiguous = MN-major, boxes of 64 x 64) with TMA into a
+// 6-stage ring whose completion is signalled on the even CTA's barriers; the even CTA
+// issues the MMAs.  Each CTA's 4 epilogue warps drain its 128 x bn accumulator (TMEM,
+// double-buffered), round to bf16, and scatter each row's 64-column chunk to its
+// (page, slot) with 16-byte stores, 4 full rows of 128 bytes per warp instruction.  When
+// n_out is an odd multiple of 64, the last n tile is half empty: its missing weight
+// columns load as zeros and are not stored.
 #include "pkm_device.cuh"
 #include "pkm_internal.h"
 
@@ -19,20 +22,20 @@ namespace pkm {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kBM = 128;
-constexpr int kStages = 4;
+constexpr int kBM = 128;                      // rows per CTA (256 per pair)
+constexpr int kStages = 6;
 constexpr int kAStageBytes = kBM * 128;       // 128 rows x 64 bf16
-constexpr int kBStageBytes = 4 * 64 * 128;    // up to 4 boxes of 64 k-rows x 64 n
+constexpr int kBStageBytes = 2 * 64 * 128;    // bn/2 <= 128 columns: 2 boxes of 64 k x 64 n
 constexpr int kStageBytes = kAStageBytes + kBStageBytes;
 constexpr int kEpiWarps = 4;
 constexpr int kOutBufBytes = 32 * 128;
 constexpr uint32_t kTmemCols = 512;
 
 struct Bars {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t t_full[2];
-    uint64_t t_empty[2];
+    uint64_t full[kStages];     // even CTA: both CTAs' A and B halves of a stage landed
+    uint64_t empty[kStages];    // both CTAs: the pair's MMAs are done with a stage
+    uint64_t t_full[2];         // both CTAs: accumulator ready
+    uint64_t t_empty[2];        // even CTA: both CTAs' epilogues drained an accumulator
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -67,7 +70,7 @@ __device__ __forceinline__ int64_t kv_row_dest(const KvMatmulArgs& a, int64_t r)
            static_cast<int64_t>(pos % static_cast<uint64_t>(a.page_size)) * a.slot_stride;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     kv_matmul_kernel(const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_w, const KvMatmulArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -79,12 +82,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bn = a.bn;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int bn = a.bn;          // pair N tile
+    const int half = bn / 2;      // B columns this CTA loads
     const int KB = a.k_in / 64;
-    const int64_t T = a.total_tiles;
-    const int64_t G = gridDim.x;
-    const int64_t t_begin = T * blockIdx.x / G;
-    const int64_t t_end = T * (blockIdx.x + 1) / G;
+    const int64_t T = a.total_tiles;  // pair tiles
+    const int64_t P = gridDim.x / 2;
+    const int64_t pair = blockIdx.x / 2;
+    const int64_t t_begin = T * pair / P;
+    const int64_t t_end = T * (pair + 1) / P;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -93,15 +100,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->t_full[i], 1);
-            mbar_init(&bars->t_empty[i], kEpiWarps);
+            mbar_init(&bars->t_empty[i], 2 * kEpiWarps);
         }
         mbar_init(&bars->mma_done, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(&bars->tmem_base, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(&bars->tmem_base, kTmemCols);
+        tmem_relinquish_pair();
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tm_x);
@@ -109,56 +116,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const WaitCtl wc{&bars->abort_flag, a.status, a.timeout_ns};
 
     if (warp == 0) {
         if (lane == 0) {
+            // A rows are re-read for every n tile of their block and W by every block: both
+            // (tens of MB) are kept in L2 ahead of the scattered cache writes
             const uint64_t keep = policy_evict_last();
-            const uint32_t stage_tx = kAStageBytes + static_cast<uint32_t>(bn) * 128;
+            const uint32_t pair_tx = 2 * (kAStageBytes + static_cast<uint32_t>(half) * 128);
             uint32_t it = 0;
             bool issued[kStages] = {};
             uint32_t last_phase[kStages] = {};
             bool ok = true;
             for (int64_t t = t_begin; t < t_end && ok; ++t) {
-                const int64_t m = t / a.n_tiles;
+                const int64_t m = (t / a.n_tiles) * 2 + rank;  // this CTA's 128-row block
                 const int n = static_cast<int>(t % a.n_tiles);
                 for (int kb = 0; kb < KB; ++kb) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1;
-                    if (!mbar_wait(&bars->empty[s], ph ^ 1, wc)) {
+                    if (!mbar_wait_cluster(&bars->empty[s], ph ^ 1, wc)) {
                         ok = false;
                         break;
                     }
                     uint8_t* st = sStages + s * kStageBytes;
-                    mbar_arrive_expect_tx(&bars->full[s], stage_tx);
-                    tma_load_2d(st, &tm_x, &bars->full[s], kb * 64, static_cast<int32_t>(m * kBM));
-                    for (int j = 0; j < bn / 64; ++j)
-                        tma_load_2d_hint(st + kAStageBytes + j * 8192, &tm_w, &bars->full[s],
-                                         n * bn + j * 64, kb * 64, keep);
+                    const uint32_t full_leader = mapa_shared(smem_u32(&bars->full[s]), 0);
+                    if (leader) mbar_arrive_expect_tx(&bars->full[s], pair_tx);
+                    tma_load_2d_pair(st, &tm_x, full_leader, kb * 64,
+                                     static_cast<int32_t>(m * kBM), keep);
+                    for (int j = 0; j < half / 64; ++j)
+                        tma_load_2d_pair(st + kAStageBytes + j * 8192, &tm_w, full_leader,
+                                         n * bn + static_cast<int>(rank) * half + j * 64,
+                                         kb * 64, keep);
                     issued[s] = true;
                     last_phase[s] = ph;
                     ++it;
                 }
             }
             if (!ok) {
-                for (int s = 0; s < kStages; ++s)
-                    if (issued[s]) mbar_wait(&bars->full[s], last_phase[s], wc, false);
+                if (leader) {
+                    for (int s = 0; s < kStages; ++s)
+                        if (issued[s]) mbar_wait_cluster(&bars->full[s], last_phase[s], wc, false);
+                } else {
+                    spin_ns(50000);
+                }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(128, bn, false, true);
+        if (leader && lane == 0) {
+            const uint32_t idesc = idesc_bf16(256, bn, false, true);
             uint32_t it = 0, tile_i = 0;
             bool ok = true;
             for (int64_t t = t_begin; t < t_end && ok; ++t) {
                 const uint32_t acc = tile_i & 1, aph = (tile_i >> 1) & 1;
-                if (!mbar_wait(&bars->t_empty[acc], aph ^ 1, wc)) break;
+                if (!mbar_wait_cluster(&bars->t_empty[acc], aph ^ 1, wc)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + acc * static_cast<uint32_t>(bn);
                 for (int kb = 0; kb < KB; ++kb) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1;
-                    if (!mbar_wait(&bars->full[s], ph, wc)) {
+                    if (!mbar_wait_cluster(&bars->full[s], ph, wc)) {
                         ok = false;
                         break;
                     }
@@ -167,27 +184,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t b_addr = a_addr + kAStageBytes;
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_bf16(d, sdesc_sw128(a_addr + k * 32, 16, 1024),
-                                 sdesc_sw128(b_addr + k * 2048, 8192, 1024), idesc,
-                                 (kb | k) != 0 ? 1u : 0u);
-                    mma_commit(&bars->empty[s]);
+                        mma_bf16_pair(d, sdesc_sw128(a_addr + k * 32, 16, 1024),
+                                      sdesc_sw128(b_addr + k * 2048, 8192, 1024), idesc,
+                                      (kb | k) != 0 ? 1u : 0u);
+                    mma_commit_pair(&bars->empty[s], 3);
                     ++it;
                 }
                 if (!ok) break;
-                mma_commit(&bars->t_full[acc]);
+                mma_commit_pair(&bars->t_full[acc], 3);
                 ++tile_i;
             }
-            mma_commit(&bars->mma_done);
-            mbar_wait(&bars->mma_done, 0, wc, false);
+            mma_commit_pair(&bars->mma_done, 1);
+            mbar_wait_cluster(&bars->mma_done, 0, wc, false);
         }
     } else {
         const int q = warp & 3;
         uint8_t* stage = sOut + q * kOutBufBytes;
         const uint32_t stage_addr = smem_u32(stage);
+        const uint32_t t_empty_leader = mapa_shared(smem_u32(&bars->t_empty[0]), 0);
         uint32_t tile_i = 0;
         int64_t cur_m = -1, my_dst = -1;
         for (int64_t t = t_begin; t < t_end; ++t) {
-            const int64_t m = t / a.n_tiles;
+            const int64_t m = (t / a.n_tiles) * 2 + rank;
             const int n = static_cast<int>(t % a.n_tiles);
             if (m != cur_m) {
                 cur_m = m;
@@ -195,11 +213,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (my_dst == -2) report(a.status, PKM_ERR_OUT_OF_RANGE);
             }
             const uint32_t acc = tile_i & 1, ph = (tile_i >> 1) & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars->t_full[acc], ph, wc))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&bars->t_full[acc], ph, wc))) break;
             tc_fence_after();
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(bn);
             for (int c = 0; c < bn / 64; ++c) {
+                const int col0 = n * bn + c * 64;
+                if (col0 >= a.n_out) break;  // padded half of the last n tile
                 uint32_t v0[32], v1[32];
                 tmem_ld_x32(tbase + c * 64, v0);
                 tmem_ld_x32(tbase + c * 64 + 32, v1);
@@ -218,7 +238,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  p[4 * j + 2], p[4 * j + 3]);
                 __syncwarp();
                 // 64 output columns of one chunk lie entirely in the K or the V plane
-                const int col0 = n * bn + c * 64;
                 const int64_t plane = col0 < a.head_elems ? 0 : a.kv_stride;
                 const int colp = (col0 < a.head_elems ? col0 : col0 - a.head_elems) + (lane & 7) * 8;
 #pragma unroll
@@ -232,15 +251,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->t_empty[acc]);
+            if (lane == 0) mbar_arrive_cluster(t_empty_leader + acc * sizeof(uint64_t));
             ++tile_i;
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -251,9 +271,10 @@ cudaError_t launch_kv_matmul(const CUtensorMap& tm_x, const CUtensorMap& tm_w, K
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    const int64_t grid = args.total_tiles < num_sms ? args.total_tiles : num_sms;
-    kv_matmul_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tm_x, tm_w,
-                                                                                    args);
+    const int64_t max_pairs = num_sms / 2;
+    const int64_t pairs = args.total_tiles < max_pairs ? args.total_tiles : max_pairs;
+    kv_matmul_kernel<<<static_cast<unsigned>(2 * pairs), kThreads, kSmemBytes, stream>>>(
+        tm_x, tm_w, args);
     return cudaGetLastError();
 }
 
