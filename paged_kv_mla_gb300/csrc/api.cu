@@ -83,10 +83,23 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, ui
            CUDA_SUCCESS;
 }
 
-int pick_bn(int n_out) {
-    if (n_out % 256 == 0) return 256;
-    if (n_out % 128 == 0) return 128;
-    return 64;
+// A row-major matrix [rows, K] viewed as k-blocks: 3-D tensor {inner = K elements of one
+// k-block, rows, k-blocks} with strides {row pitch, k-block pitch} (the k-block dimension
+// steps inside a row), boxes of {inner, box_rows, box_kblocks}.  One box lands in shared
+// memory as box_kblocks consecutive [box_rows x inner] tiles, each 128-byte swizzled.
+bool encode_kblocks_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                       uint64_t inner, uint64_t rows, uint64_t kblocks, uint64_t row_pitch_bytes,
+                       uint64_t kblock_pitch_bytes, uint32_t box_rows, uint32_t box_kblocks) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[3] = {inner, rows, kblocks};
+    const cuuint64_t strides[2] = {row_pitch_bytes, kblock_pitch_bytes};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(inner), box_rows, box_kblocks};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
 }
 
 // Checks shared by both decompress entry points.  Returns PKM_OK or the error.
@@ -185,13 +198,14 @@ pkm_status mla_decompress_k_paged(const pkm_paged_cache* cache, uint32_t layer_i
                                      k_latent_buffer, k_buffer);
     if (st != PKM_OK) return st;
     if (kv_lora_rank % 64 != 0 || kv_lora_rank > 512 || n_out % 64 != 0) return PKM_ERR_UNSUPPORTED;
-    const int bn = pick_bn(n_out);
+    // CTA-pair tiles of 256 rows x bn columns (the widest of 256 / 128 / 64 dividing
+    // n_out); each CTA loads bn/2 W_k rows per k-block
+    const int bn = (n_out % 256 == 0) ? 256 : (n_out % 128 == 0) ? 128 : 64;
     DecompressArgs a = make_decompress_args(cache, layer_idx, buffer_row_offsets, cache_offsets,
                                             batch, buffer_length, kv_lora_rank, rope_dim, n_out,
                                             k_latent_buffer, k_buffer, dev_status, bn);
     int sms = 0;
     if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
-    // CTA-pair tiles: 256 rows (128 per CTA) x bn columns; each CTA loads bn/2 W_k rows
     a.m_tiles = (buffer_length + 255) / 256;
     a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
     alignas(64) CUtensorMap tm_w, tm_k;
@@ -238,6 +252,8 @@ pkm_status mla_decompress_k_paged_fp8(const pkm_paged_cache* cache, uint32_t lay
     DecompressArgs a = make_decompress_args(cache, layer_idx, buffer_row_offsets, cache_offsets,
                                             batch, buffer_length, kv_lora_rank, rope_dim, n_out,
                                             k_latent_buffer, k_buffer, dev_status, 128);
+    a.m_tiles = (buffer_length + 255) / 256;  // CTA-pair tiles of 256 rows
+    a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
     Fp8Extra x{};
     x.q_latent = static_cast<uint8_t*>(workspace);
     x.q_scale = reinterpret_cast<float*>(
@@ -249,8 +265,9 @@ pkm_status mla_decompress_k_paged_fp8(const pkm_paged_cache* cache, uint32_t lay
     alignas(64) CUtensorMap tm_q, tm_w, tm_k;
     if (!encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.q_latent, kv_lora_rank, buffer_length,
                    static_cast<uint64_t>(kv_lora_rank), 128, 128) ||
-        !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_k_e4m3, kv_lora_rank, n_out,
-                   static_cast<uint64_t>(kv_lora_rank), 128, 128) ||
+        !encode_kblocks_3d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_k_e4m3, 128, n_out,
+                           kv_lora_rank / 128, static_cast<uint64_t>(kv_lora_rank), 128, 64,
+                           kv_lora_rank / 128) ||
         !encode_2d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_buffer, n_out, buffer_length,
                    static_cast<uint64_t>(n_out) * 2, 64, 32))
         return PKM_ERR_CUDA;

@@ -16,8 +16,9 @@
 //
 // Each pair walks a contiguous range of tile ids (m_pair * n_tiles + n), so consecutive
 // tiles reuse the gathered rows.  Warp roles, in both CTAs:
-//   warp 0      TMA producer: this CTA's half of W_k [bn/2 x 64] (128-byte swizzle) into a
-//               5-stage ring; completion is signalled on the even CTA's barrier.
+//   warps 0, 8  TMA producers: this CTA's half of W_k [bn/2 x 64] (128-byte swizzle) into a
+//               5-stage ring, alternate stages each; completion is signalled on the even
+//               CTA's barrier.
 //   warp 1      TMEM allocator (pair); in the even CTA also the single MMA-issuing thread.
 //   warps 2-3   gatherers: resolve rows through buffer_row_offsets / cache_offsets / the
 //               page table, cp.async the nope columns into the swizzled A tile (one group
@@ -32,7 +33,7 @@
 namespace pkm {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;                // 9 warps: + a second W_k producer
 constexpr int kBM = 128;                     // rows per CTA (256 per pair)
 constexpr int kKBMax = 8;                    // kv_lora_rank <= 512 = 8 k-blocks of 64
 constexpr int kABlockBytes = kBM * 128;      // 16 KB per k-block
@@ -121,9 +122,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const WaitCtl wc{&bars->abort_flag, a.status, a.timeout_ns};
     const int64_t row_end = decompress_row_end(a);
 
-    if (warp == 0) {
-        // ---------------- W_k producer (this CTA's half of each tile) ----------------
+    if (warp == 0 || warp == 8) {
+        // ---------------- W_k producers (this CTA's half of each tile) ----------------
+        // Two threads issue alternate ring iterations: a TMA load costs its issuing thread a
+        // roughly fixed time, so one thread could not keep up with the MMAs.
         if (lane == 0) {
+            const uint32_t who = warp == 0 ? 0u : 1u;
             const uint64_t keep = policy_evict_last();
             uint32_t it = 0;
             bool issued[kStages] = {};
@@ -131,7 +135,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int64_t t = t_begin; t < t_end && ok; ++t) {
                 const int n = static_cast<int>(t % a.n_tiles);
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    if ((it & 1u) != who) continue;
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1;
                     if (!mbar_wait_cluster(&bars->b_empty[s], ph ^ 1, wc)) {
                         ok = false;
@@ -144,7 +149,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                      n * bn + static_cast<int>(rank) * half, keep);
                     issued[s] = true;
                     last_phase[s] = ph;
-                    ++it;
                 }
             }
             if (!ok) {  // let loads already in flight land before the CTA retires
@@ -275,7 +279,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ++seg;
         }
         cp_async_wait<0>();
-    } else {
+    } else if (warp < 8) {
         // ---------------- epilogue (this CTA's 128 rows) ----------------
         const int q = warp & 3;  // TMEM lane quarter == 32-row slab of the CTA's rows
         const uint32_t t_empty_leader = mapa_shared(smem_u32(&bars->t_empty[0]), 0);
@@ -335,7 +339,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(t_empty_leader + acc * sizeof(uint64_t));
+            if (lane == 0) mbar_arrive_remote(t_empty_leader + acc * sizeof(uint64_t));
             ++tile_i;
         }
         if (lane == 0) bulk_wait<0>();

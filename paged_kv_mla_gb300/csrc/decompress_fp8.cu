@@ -12,14 +12,16 @@
 //      loads/stores, and quantises its first kv_lora_rank columns per 128-column block
 //      (s = amax / 448, q = e4m3_rne_satfinite(x / s), fp32) into the workspace.  Every
 //      row is quantised exactly once, however many n tiles later consume it.
-//   2. decompress_fp8_gemm_kernel: persistent CTAs over 128 x 128 output tiles (one n
-//      tile = one weight-scale block).  TMA brings the quantised A tile (resident for the
-//      CTA's range segment) and W_k blocks of 128 x 128 e4m3 through an 8-stage ring;
-//      tcgen05.mma kind::f8f6f4 accumulates each 128-wide k-block into its own TMEM
-//      accumulator (4 x 128 columns), and 8 epilogue warps combine them in registers as
-//      sum_kb (s_a[row, kb] * s_w[n_tile, kb]) * acc_kb before rounding to bf16 and
-//      TMA-storing k_buffer.  An accumulator is released as soon as the epilogue has read
-//      it, so the next tile's MMAs overlap the rest of the epilogue.
+//   2. decompress_fp8_gemm_kernel: clusters of two CTAs (a CTA pair) over 256 x 128 output
+//      tiles (one n tile = one weight-scale block).  Each CTA brings its 128 rows of the
+//      quantised A tile (resident for the pair's range segment) and its 64-row half of the
+//      tile's 128 x kv_lora_rank e4m3 W_k slice (one 3-D TMA operation, all k-blocks) into a
+//      4-tile ring; the even CTA issues
+//      tcgen05.mma.cta_group::2 kind::f8f6f4 (M = 256), accumulating each 128-wide k-block
+//      into its own TMEM accumulator (4 x 128 columns per CTA).  8 epilogue warps per CTA
+//      combine them in registers as sum_kb (s_a[row, kb] * s_w[n_tile, kb]) * acc_kb before
+//      rounding to bf16 and TMA-storing k_buffer.  An accumulator is released as soon as
+//      the epilogue has read it, so the next tile's MMAs overlap the rest of the epilogue.
 #include "pkm_device.cuh"
 #include "pkm_internal.h"
 
@@ -95,23 +97,24 @@ __global__ void __launch_bounds__(256)
 // ------------------------------------------------------------------------------------
 
 constexpr int kThreads = 320;                 // producer, MMA, 8 epilogue warps
-constexpr int kBM = 128;
-constexpr int kBN = 128;
+constexpr int kBM = 128;                      // rows per CTA (256 per pair)
+constexpr int kBN = 128;                      // pair N tile = one weight-scale block
 constexpr int kKBMax = 4;                     // kv_lora_rank <= 512
 constexpr int kABlockBytes = kBM * 128;       // 128 rows x 128 e4m3
-constexpr int kStages = 8;
-constexpr int kBStageBytes = kBN * 128;
+constexpr int kStages = 4;
+constexpr int kBKBlockBytes = (kBN / 2) * 128;        // this CTA's 64 weight rows x 128 e4m3
+constexpr int kBStageBytes = kKBMax * kBKBlockBytes;  // a tile's weight half: 32 KB
 constexpr int kEpiWarps = 8;
 constexpr int kOutBufBytes = 32 * 128;
 constexpr uint32_t kTmemCols = 512;           // kKBMax accumulators x 128 columns
 
 struct Bars {
-    uint64_t b_full[kStages];
-    uint64_t b_empty[kStages];
-    uint64_t a_full;
-    uint64_t a_empty;
-    uint64_t t_full[kKBMax];
-    uint64_t t_empty[kKBMax];
+    uint64_t b_full[kStages];   // even CTA: both halves of a W_k stage landed
+    uint64_t b_empty[kStages];  // both CTAs: the pair's MMAs are done with a stage
+    uint64_t a_full;            // even CTA: both CTAs' A tiles landed
+    uint64_t a_empty;           // both CTAs: the MMAs are done with A
+    uint64_t t_full[kKBMax];    // both CTAs: k-block accumulator ready
+    uint64_t t_empty[kKBMax];   // even CTA: both CTAs' epilogues read a k-block accumulator
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -124,7 +127,18 @@ constexpr size_t kOffBars = kOffOut + size_t(kEpiWarps) * kOutBufBytes;
 constexpr size_t kSmemBytes = kOffBars + sizeof(Bars) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Pair MMA, e4m3 x e4m3 -> fp32 (M = 256 over the two CTAs).
+__device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decompress_fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_q,
                                const __grid_constant__ CUtensorMap tm_w,
                                const __grid_constant__ CUtensorMap tm_kbuf,
@@ -139,11 +153,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
     const int KB = a.kv_lora_rank / 128;
-    const int64_t T = a.total_tiles;
-    const int64_t G = gridDim.x;
-    const int64_t t_begin = T * blockIdx.x / G;
-    const int64_t t_end = T * (blockIdx.x + 1) / G;
+    const int64_t T = a.total_tiles;  // pair tiles
+    const int64_t P = gridDim.x / 2;
+    const int64_t pair = blockIdx.x / 2;
+    const int64_t t_begin = T * pair / P;
+    const int64_t t_end = T * (pair + 1) / P;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -154,15 +171,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->a_empty, 1);
         for (int i = 0; i < kKBMax; ++i) {
             mbar_init(&bars->t_full[i], 1);
-            mbar_init(&bars->t_empty[i], kEpiWarps);
+            mbar_init(&bars->t_empty[i], 2 * kEpiWarps);
         }
         mbar_init(&bars->mma_done, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(&bars->tmem_base, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(&bars->tmem_base, kTmemCols);
+        tmem_relinquish_pair();
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tm_q);
@@ -171,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const WaitCtl wc{&bars->abort_flag, a.status, a.timeout_ns};
@@ -179,51 +197,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t keep = policy_evict_last();
+            const uint32_t a_full_leader = mapa_shared(smem_u32(&bars->a_full), 0);
             uint32_t it = 0, seg = 0;
             int64_t cur_m = -1;
-            bool issued[kStages] = {};
-            uint32_t last_phase[kStages] = {};
-            bool a_issued = false;
-            uint32_t a_phase = 0;
             bool ok = true;
             for (int64_t t = t_begin; t < t_end && ok; ++t) {
-                const int64_t m = t / a.n_tiles;
+                const int64_t m_pair = t / a.n_tiles;
                 const int n = static_cast<int>(t % a.n_tiles);
-                if (m != cur_m) {
-                    cur_m = m;
-                    if (seg > 0 && !mbar_wait(&bars->a_empty, (seg - 1) & 1, wc)) break;
-                    mbar_arrive_expect_tx(&bars->a_full,
-                                          static_cast<uint32_t>(KB) * kABlockBytes);
+                if (m_pair != cur_m) {
+                    cur_m = m_pair;
+                    if (seg > 0 && !mbar_wait_cluster(&bars->a_empty, (seg - 1) & 1, wc)) break;
+                    if (leader)
+                        mbar_arrive_expect_tx(&bars->a_full,
+                                              2u * static_cast<uint32_t>(KB) * kABlockBytes);
                     for (int kb = 0; kb < KB; ++kb)
-                        tma_load_2d(sA + kb * kABlockBytes, &tm_q, &bars->a_full, kb * 128,
-                                    static_cast<int32_t>(m * kBM));
-                    a_issued = true;
-                    a_phase = seg & 1;
+                        tma_load_2d_pair(sA + kb * kABlockBytes, &tm_q, a_full_leader, kb * 128,
+                                         static_cast<int32_t>((m_pair * 2 + rank) * kBM), keep);
                     ++seg;
                 }
-                for (int kb = 0; kb < KB; ++kb) {
+                {  // one 3-D operation: all k-blocks of this CTA's 64 weight rows
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1;
-                    if (!mbar_wait(&bars->b_empty[s], ph ^ 1, wc)) {
+                    if (!mbar_wait_cluster(&bars->b_empty[s], ph ^ 1, wc)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&bars->b_full[s], kBStageBytes);
-                    tma_load_2d_hint(sB + s * kBStageBytes, &tm_w, &bars->b_full[s], kb * 128,
-                                     n * kBN, keep);
-                    issued[s] = true;
-                    last_phase[s] = ph;
+                    if (leader)
+                        mbar_arrive_expect_tx(&bars->b_full[s],
+                                              2u * static_cast<uint32_t>(KB) * kBKBlockBytes);
+                    tma_load_3d_pair(sB + s * kBStageBytes, &tm_w,
+                                     mapa_shared(smem_u32(&bars->b_full[s]), 0), 0,
+                                     n * kBN + static_cast<int>(rank) * (kBN / 2), 0, keep);
                     ++it;
                 }
             }
-            if (bars->abort_flag) {
-                for (int s = 0; s < kStages; ++s)
-                    if (issued[s]) mbar_wait(&bars->b_full[s], last_phase[s], wc, false);
-                if (a_issued) mbar_wait(&bars->a_full, a_phase, wc, false);
-            }
+            if (bars->abort_flag) spin_ns(50000);  // let loads in flight land before retiring
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = idesc_e4m3(128, kBN);
+        if (leader && lane == 0) {
+            const uint32_t idesc = idesc_e4m3(256, kBN);
             uint32_t it = 0, tile_i = 0, seg = 0;
             int64_t cur_m = -1;
             bool ok = true;
@@ -231,38 +242,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t m = t / a.n_tiles;
                 if (m != cur_m) {
                     if (cur_m >= 0) {
-                        mma_commit(&bars->a_empty);
+                        mma_commit_pair(&bars->a_empty, 3);
                         ++seg;
                     }
                     cur_m = m;
-                    if (!mbar_wait(&bars->a_full, seg & 1, wc)) break;
+                    if (!mbar_wait_cluster(&bars->a_full, seg & 1, wc)) break;
                 }
+                const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+                if (!mbar_wait_cluster(&bars->b_full[s], ph, wc)) break;
+                const uint32_t b_stage = smem_u32(sB + s * kBStageBytes);
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&bars->t_empty[kb], (tile_i & 1) ^ 1, wc)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t s = it % kStages, ph = (it / kStages) & 1;
-                    if (!mbar_wait(&bars->b_full[s], ph, wc)) {
+                    if (!mbar_wait_cluster(&bars->t_empty[kb], (tile_i & 1) ^ 1, wc)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(sA + kb * kABlockBytes);
-                    const uint32_t b_addr = smem_u32(sB + s * kBStageBytes);
+                    const uint32_t b_addr = b_stage + kb * kBKBlockBytes;
                     const uint32_t d = tmem + static_cast<uint32_t>(kb) * kBN;
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_e4m3(d, sdesc_sw128(a_addr + k * 32, 16, 1024),
-                                 sdesc_sw128(b_addr + k * 32, 16, 1024), idesc, k != 0 ? 1u : 0u);
-                    mma_commit(&bars->b_empty[s]);
-                    mma_commit(&bars->t_full[kb]);
-                    ++it;
+                        mma_e4m3_pair(d, sdesc_sw128(a_addr + k * 32, 16, 1024),
+                                      sdesc_sw128(b_addr + k * 32, 16, 1024), idesc,
+                                      k != 0 ? 1u : 0u);
+                    mma_commit_pair(&bars->t_full[kb], 3);
                 }
+                mma_commit_pair(&bars->b_empty[s], 3);
+                ++it;
                 ++tile_i;
             }
-            mma_commit(&bars->mma_done);
-            mbar_wait(&bars->mma_done, 0, wc, false);
+            mma_commit_pair(&bars->mma_done, 1);
+            mbar_wait_cluster(&bars->mma_done, 0, wc, false);
         }
     } else {
         // 8 epilogue warps: warp w reads TMEM lane quarter w % 4 (32 rows) and one 64-column
@@ -271,16 +281,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
         uint8_t* stage = sOut + (warp - 2) * kOutBufBytes;
+        const uint32_t t_empty_leader = mapa_shared(smem_u32(&bars->t_empty[0]), 0);
         uint32_t tile_i = 0;
-        int64_t cur_m = -1, my_row = 0;
+        int64_t cur_m = -1, my_row = 0, m = 0;
         bool slab_full = false, my_valid = false;
         float sa[kKBMax] = {0.f, 0.f, 0.f, 0.f};
         bool ok = true;
         for (int64_t t = t_begin; t < t_end && ok; ++t) {
-            const int64_t m = t / a.n_tiles;
+            const int64_t m_pair = t / a.n_tiles;
             const int n = static_cast<int>(t % a.n_tiles);
-            if (m != cur_m) {
-                cur_m = m;
+            if (m_pair != cur_m) {
+                cur_m = m_pair;
+                m = m_pair * 2 + rank;
                 my_row = m * kBM + q * 32 + lane;
                 my_valid = decompress_row_source(a, my_row, row_end) >= 0;
                 slab_full = __all_sync(0xffffffffu, my_valid);
@@ -294,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kb = 0; kb < kKBMax; ++kb) {
                 if (kb >= KB) break;
-                if (!__all_sync(0xffffffffu, mbar_wait(&bars->t_full[kb], tile_i & 1, wc))) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_cluster(&bars->t_full[kb], tile_i & 1, wc))) {
                     ok = false;
                     break;
                 }
@@ -308,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->t_empty[kb]);
+                if (lane == 0) mbar_arrive_remote(t_empty_leader + kb * sizeof(uint64_t));
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     acc[j] = fmaf(cs, __uint_as_float(v0[j]), acc[j]);
@@ -348,8 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -372,8 +386,9 @@ cudaError_t launch_decompress_fp8_gemm(const CUtensorMap& tm_q, const CUtensorMa
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    const int64_t grid = args.total_tiles < num_sms ? args.total_tiles : num_sms;
-    decompress_fp8_gemm_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
+    const int64_t max_pairs = num_sms / 2;
+    const int64_t pairs = args.total_tiles < max_pairs ? args.total_tiles : max_pairs;
+    decompress_fp8_gemm_kernel<<<static_cast<unsigned>(2 * pairs), kThreads, kSmemBytes, stream>>>(
         tm_q, tm_w, tm_kbuf, args, extra);
     return cudaGetLastError();
 }

@@ -251,7 +251,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(t_empty_leader + acc * sizeof(uint64_t));
+            if (lane == 0) mbar_arrive_remote(t_empty_leader + acc * sizeof(uint64_t));
             ++tile_i;
         }
     }
