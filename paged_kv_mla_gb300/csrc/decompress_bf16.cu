@@ -138,7 +138,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     if ((it & 1u) != who) continue;
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1;
-                    if (!mbar_wait_cluster(&bars->b_empty[s], ph ^ 1, wc)) {
+                    if (!mbar_wait(&bars->b_empty[s], ph ^ 1, wc)) {
                         ok = false;
                         break;
                     }
@@ -154,7 +154,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok) {  // let loads already in flight land before the CTA retires
                 if (leader) {
                     for (int s = 0; s < kStages; ++s)
-                        if (issued[s]) mbar_wait_cluster(&bars->b_full[s], last_phase[s], wc, false);
+                        if (issued[s]) mbar_wait(&bars->b_full[s], last_phase[s], wc, false);
                 } else {
                     spin_ns(50000);
                 }
@@ -178,7 +178,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     cur_m = m;
                 }
                 const uint32_t acc = tile_i & 1, aph = (tile_i >> 1) & 1;
-                if (!mbar_wait_cluster(&bars->t_empty[acc], aph ^ 1, wc)) break;
+                if (!mbar_wait(&bars->t_empty[acc], aph ^ 1, wc)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + acc * static_cast<uint32_t>(bn);
                 for (int kb = 0; kb < KB; ++kb) {
@@ -187,7 +187,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1;
-                    if (!mbar_wait_cluster(&bars->b_full[s], ph, wc)) {
+                    if (!mbar_wait(&bars->b_full[s], ph, wc)) {
                         ok = false;
                         break;
                     }
@@ -207,7 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 ++tile_i;
             }
             mma_commit_pair(&bars->mma_done, 1);
-            mbar_wait_cluster(&bars->mma_done, 0, wc, false);
+            mbar_wait(&bars->mma_done, 0, wc, false);
         }
     } else if (warp < 4) {
         // ---------------- gatherers (this CTA's 128 rows) ----------------
@@ -230,7 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             if (g == 0)
                 bars->gather_go =
-                    (seg == 0 || mbar_wait_cluster(&bars->a_empty, (seg - 1) & 1, wc)) ? 1 : 0;
+                    (seg == 0 || mbar_wait(&bars->a_empty, (seg - 1) & 1, wc)) ? 1 : 0;
             named_bar_sync(1, kGatherThreads);
             if (!bars->gather_go) break;
             for (int kb = 0; kb < KB; ++kb) {
@@ -297,7 +297,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 slab_full = __all_sync(0xffffffffu, my_valid);
             }
             const uint32_t acc = tile_i & 1, ph = (tile_i >> 1) & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&bars->t_full[acc], ph, wc))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->t_full[acc], ph, wc))) break;
             tc_fence_after();
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(bn);

@@ -206,7 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int n = static_cast<int>(t % a.n_tiles);
                 if (m_pair != cur_m) {
                     cur_m = m_pair;
-                    if (seg > 0 && !mbar_wait_cluster(&bars->a_empty, (seg - 1) & 1, wc)) break;
+                    if (seg > 0 && !mbar_wait(&bars->a_empty, (seg - 1) & 1, wc)) break;
                     if (leader)
                         mbar_arrive_expect_tx(&bars->a_full,
                                               2u * static_cast<uint32_t>(KB) * kABlockBytes);
@@ -217,7 +217,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 {  // one 3-D operation: all k-blocks of this CTA's 64 weight rows
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1;
-                    if (!mbar_wait_cluster(&bars->b_empty[s], ph ^ 1, wc)) {
+                    if (!mbar_wait(&bars->b_empty[s], ph ^ 1, wc)) {
                         ok = false;
                         break;
                     }
@@ -246,13 +246,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         ++seg;
                     }
                     cur_m = m;
-                    if (!mbar_wait_cluster(&bars->a_full, seg & 1, wc)) break;
+                    if (!mbar_wait(&bars->a_full, seg & 1, wc)) break;
                 }
                 const uint32_t s = it % kStages, ph = (it / kStages) & 1;
-                if (!mbar_wait_cluster(&bars->b_full[s], ph, wc)) break;
+                if (!mbar_wait(&bars->b_full[s], ph, wc)) break;
                 const uint32_t b_stage = smem_u32(sB + s * kBStageBytes);
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait_cluster(&bars->t_empty[kb], (tile_i & 1) ^ 1, wc)) {
+                    if (!mbar_wait(&bars->t_empty[kb], (tile_i & 1) ^ 1, wc)) {
                         ok = false;
                         break;
                     }
@@ -272,7 +272,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 ++tile_i;
             }
             mma_commit_pair(&bars->mma_done, 1);
-            mbar_wait_cluster(&bars->mma_done, 0, wc, false);
+            mbar_wait(&bars->mma_done, 0, wc, false);
         }
     } else {
         // 8 epilogue warps: warp w reads TMEM lane quarter w % 4 (32 rows) and one 64-column
@@ -307,7 +307,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int kb = 0; kb < kKBMax; ++kb) {
                 if (kb >= KB) break;
                 if (!__all_sync(0xffffffffu,
-                                mbar_wait_cluster(&bars->t_full[kb], tile_i & 1, wc))) {
+                                mbar_wait(&bars->t_full[kb], tile_i & 1, wc))) {
                     ok = false;
                     break;
                 }

@@ -136,7 +136,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int n = static_cast<int>(t % a.n_tiles);
                 for (int kb = 0; kb < KB; ++kb) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1;
-                    if (!mbar_wait_cluster(&bars->empty[s], ph ^ 1, wc)) {
+                    if (!mbar_wait(&bars->empty[s], ph ^ 1, wc)) {
                         ok = false;
                         break;
                     }
@@ -157,7 +157,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok) {
                 if (leader) {
                     for (int s = 0; s < kStages; ++s)
-                        if (issued[s]) mbar_wait_cluster(&bars->full[s], last_phase[s], wc, false);
+                        if (issued[s]) mbar_wait(&bars->full[s], last_phase[s], wc, false);
                 } else {
                     spin_ns(50000);
                 }
@@ -170,12 +170,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int64_t t = t_begin; t < t_end && ok; ++t) {
                 const uint32_t acc = tile_i & 1, aph = (tile_i >> 1) & 1;
-                if (!mbar_wait_cluster(&bars->t_empty[acc], aph ^ 1, wc)) break;
+                if (!mbar_wait(&bars->t_empty[acc], aph ^ 1, wc)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + acc * static_cast<uint32_t>(bn);
                 for (int kb = 0; kb < KB; ++kb) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1;
-                    if (!mbar_wait_cluster(&bars->full[s], ph, wc)) {
+                    if (!mbar_wait(&bars->full[s], ph, wc)) {
                         ok = false;
                         break;
                     }
@@ -195,7 +195,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 ++tile_i;
             }
             mma_commit_pair(&bars->mma_done, 1);
-            mbar_wait_cluster(&bars->mma_done, 0, wc, false);
+            mbar_wait(&bars->mma_done, 0, wc, false);
         }
     } else {
         const int q = warp & 3;
@@ -213,7 +213,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (my_dst == -2) report(a.status, PKM_ERR_OUT_OF_RANGE);
             }
             const uint32_t acc = tile_i & 1, ph = (tile_i >> 1) & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&bars->t_full[acc], ph, wc))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->t_full[acc], ph, wc))) break;
             tc_fence_after();
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(bn);

@@ -81,13 +81,10 @@ struct WaitCtl {
     uint64_t timeout_ns;
 };
 
-// Waits until the phase with the given parity of `bar` has completed.  Returns false when
-// another role raised the abort flag (if `obey_abort`) or when the wait outlived
-// timeout_ns; in the latter case it records PKM_ERR_TIMEOUT and raises the abort flag so
-// that every role of the CTA winds down.
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w,
-                                       bool obey_abort = true) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait: spins until the phase completes, the abort flag rises or the wait
+// outlives timeout_ns.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                                   const WaitCtl& w, bool obey_abort) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -100,6 +97,22 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, co
             }
         }
     }
+}
+
+// Waits until the phase with the given parity of `bar` has completed (acquire, CTA scope).
+// Returns false when another role raised the abort flag (if `obey_abort`) or when the wait
+// outlived timeout_ns; in the latter case it records PKM_ERR_TIMEOUT and raises the abort
+// flag so that every role of the CTA winds down.
+//
+// CTA scope is enough for every barrier whose phase is completed by the asynchronous proxy
+// (TMA complete_tx, tcgen05.commit) or by arrivals that only hand over tensor-memory
+// accumulators ordered with tcgen05 fences, including arrivals from the other CTA of a pair.
+// A satisfied wait then costs a few tens of cycles, against several hundred for the
+// cluster-scope acquire of mbar_wait_cluster.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w,
+                                          bool obey_abort = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, w, obey_abort);
 }
 
 // ------------------------------------------------------------------------------------
@@ -146,8 +159,9 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
     return ok != 0;
 }
 
-// mbar_wait for barriers that receive arrivals from the other CTA of a pair (acquire at
-// cluster scope).  Same limits and abort behaviour as mbar_wait.
+// mbar_wait with acquire at cluster scope, for a barrier whose completion publishes ordinary
+// (generic-proxy) shared-memory writes made by threads of the other CTA of the pair.  Same
+// limits and abort behaviour as mbar_wait.
 static __device__ __noinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
                                                       const WaitCtl& w, bool obey_abort = true) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
