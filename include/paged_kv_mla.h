@@ -121,6 +121,10 @@ typedef struct {
  *   n_out                num_heads * qk_nope_head_dim: a multiple of 64.
  *   k_latent_buffer      device bf16 [buffer_length, C], row-major, 16-byte aligned.
  *   k_buffer             device bf16 [buffer_length, n_out], row-major, 16-byte aligned.
+ *
+ * Returns PKM_ERR_UNSUPPORTED (launching nothing) when one layer of the cache spans
+ * 2^35 - 64 elements (about 64 GiB) or more: the kernel keeps row addresses as 32-bit
+ * counts of 16-byte units inside the layer.
  */
 pkm_status mla_decompress_k_paged(const pkm_paged_cache* cache, uint32_t layer_idx,
                                   const uint32_t* buffer_row_offsets,

@@ -102,6 +102,28 @@ bool encode_kblocks_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
            CUDA_SUCCESS;
 }
 
+// One layer of the paged latent cache as a 4-D tensor {64 columns of a k-block, slot, page,
+// k-block} (strides slot_stride, page_stride and 128 bytes), boxes of {64, 8 slots, 1 page,
+// kblocks}: one box is eight consecutive slots of one page with all their k-blocks, landing
+// as kblocks 1 KB tiles of [8 rows x 128 bytes], 128-byte swizzled.
+bool encode_cache_gather(CUtensorMap* map, const void* layer, int32_t page_size,
+                         int32_t num_pages, int32_t kblocks, int64_t slot_stride,
+                         int64_t page_stride) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(page_size),
+                                static_cast<cuuint64_t>(num_pages),
+                                static_cast<cuuint64_t>(kblocks)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(slot_stride) * 2,
+                                   static_cast<cuuint64_t>(page_stride) * 2, 128};
+    const cuuint32_t box[4] = {64, 8, 1, static_cast<cuuint32_t>(kblocks)};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(layer), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 // Checks shared by both decompress entry points.  Returns PKM_OK or the error.
 pkm_status check_decompress(const pkm_paged_cache* cache, uint32_t layer_idx, const uint32_t* bro,
                             const uint32_t* co, int32_t batch, int32_t buffer_length,
@@ -198,6 +220,10 @@ pkm_status mla_decompress_k_paged(const pkm_paged_cache* cache, uint32_t layer_i
                                      k_latent_buffer, k_buffer);
     if (st != PKM_OK) return st;
     if (kv_lora_rank % 64 != 0 || kv_lora_rank > 512 || n_out % 64 != 0) return PKM_ERR_UNSUPPORTED;
+    // the kernel keeps each row's offset in the layer as a 32-bit count of 16-byte units
+    const int64_t layer_span = static_cast<int64_t>(cache->num_pages) * cache->page_stride +
+                               static_cast<int64_t>(cache->page_size) * cache->slot_stride;
+    if (layer_span >= (static_cast<int64_t>(1) << 35) - 64) return PKM_ERR_UNSUPPORTED;
     // CTA-pair tiles of 256 rows x bn columns (the widest of 256 / 128 / 64 dividing
     // n_out); each CTA loads bn/2 W_k rows per k-block
     const int bn = (n_out % 256 == 0) ? 256 : (n_out % 128 == 0) ? 128 : 64;
@@ -208,13 +234,19 @@ pkm_status mla_decompress_k_paged(const pkm_paged_cache* cache, uint32_t layer_i
     if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
     a.m_tiles = (buffer_length + 255) / 256;
     a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
-    alignas(64) CUtensorMap tm_w, tm_k;
+    alignas(64) CUtensorMap tm_w;
+    alignas(64) CUtensorMap tm_c = {};
     if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_k, kv_lora_rank, n_out,
-                   static_cast<uint64_t>(kv_lora_rank) * 2, 64, bn / 2) ||
-        !encode_2d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_buffer, n_out, buffer_length,
-                   static_cast<uint64_t>(n_out) * 2, 64, 32))
+                   static_cast<uint64_t>(kv_lora_rank) * 2, 64, bn / 2))
         return PKM_ERR_CUDA;
-    return pkm::launch_decompress_bf16(tm_w, tm_k, a, sms, static_cast<cudaStream_t>(stream)) ==
+    // Rows arriving as runs of eight slots of one page come by TMA; that needs pages of at
+    // least eight slots.  Otherwise every row takes the per-row path.
+    a.gather_tma = cache->page_size >= 8 ? 1 : 0;
+    if (a.gather_tma &&
+        !encode_cache_gather(&tm_c, a.cache_layer, cache->page_size, cache->num_pages,
+                             kv_lora_rank / 64, cache->slot_stride, cache->page_stride))
+        return PKM_ERR_CUDA;
+    return pkm::launch_decompress_bf16(tm_w, tm_c, a, sms, static_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? PKM_OK
                : PKM_ERR_CUDA;
@@ -262,18 +294,16 @@ pkm_status mla_decompress_k_paged_fp8(const pkm_paged_cache* cache, uint32_t lay
     x.w_scale = w_k_scale;
     int sms = 0;
     if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
-    alignas(64) CUtensorMap tm_q, tm_w, tm_k;
+    alignas(64) CUtensorMap tm_q, tm_w;
     if (!encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.q_latent, kv_lora_rank, buffer_length,
                    static_cast<uint64_t>(kv_lora_rank), 128, 128) ||
         !encode_kblocks_3d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_k_e4m3, 128, n_out,
                            kv_lora_rank / 128, static_cast<uint64_t>(kv_lora_rank), 128, 64,
-                           kv_lora_rank / 128) ||
-        !encode_2d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_buffer, n_out, buffer_length,
-                   static_cast<uint64_t>(n_out) * 2, 64, 32))
+                           kv_lora_rank / 128))
         return PKM_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pkm::launch_fp8_gather_quantize(a, x, sms, s) != cudaSuccess) return PKM_ERR_CUDA;
-    return pkm::launch_decompress_fp8_gemm(tm_q, tm_w, tm_k, a, x, sms, s) == cudaSuccess
+    return pkm::launch_decompress_fp8_gemm(tm_q, tm_w, a, x, sms, s) == cudaSuccess
                ? PKM_OK
                : PKM_ERR_CUDA;
 }

@@ -20,7 +20,8 @@
 //      tcgen05.mma.cta_group::2 kind::f8f6f4 (M = 256), accumulating each 128-wide k-block
 //      into its own TMEM accumulator (4 x 128 columns per CTA).  8 epilogue warps per CTA
 //      combine them in registers as sum_kb (s_a[row, kb] * s_w[n_tile, kb]) * acc_kb before
-//      rounding to bf16 and TMA-storing k_buffer.  An accumulator is released as soon as
+//      rounding to bf16 and storing k_buffer in whole 128-byte row segments (through a
+//      swizzled 4 KB shared buffer per warp).  An accumulator is released as soon as
 //      the epilogue has read it, so the next tile's MMAs overlap the rest of the epilogue.
 #include "pkm_device.cuh"
 #include "pkm_internal.h"
@@ -141,7 +142,6 @@ __device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t adesc, u
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decompress_fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_q,
                                const __grid_constant__ CUtensorMap tm_w,
-                               const __grid_constant__ CUtensorMap tm_kbuf,
                                const DecompressArgs a, const Fp8Extra x) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -184,7 +184,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tm_q);
         tma_prefetch_map(&tm_w);
-        tma_prefetch_map(&tm_kbuf);
     }
     tc_fence_before();
     __syncthreads();
@@ -280,11 +279,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // 32-column TMEM loads of a k-block before waiting once.
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
-        uint8_t* stage = sOut + (warp - 2) * kOutBufBytes;
+        const uint32_t stage = smem_u32(sOut + (warp - 2) * kOutBufBytes);
         const uint32_t t_empty_leader = mapa_shared(smem_u32(&bars->t_empty[0]), 0);
         uint32_t tile_i = 0;
-        int64_t cur_m = -1, my_row = 0, m = 0;
-        bool slab_full = false, my_valid = false;
+        int64_t cur_m = -1;
+        uint16_t* row0 = a.k_buffer;  // first row of this warp's 32-row slab
+        uint32_t valid = 0;           // bit r: slab row r is a buffer row with a source
         float sa[kKBMax] = {0.f, 0.f, 0.f, 0.f};
         bool ok = true;
         for (int64_t t = t_begin; t < t_end && ok; ++t) {
@@ -292,14 +292,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int n = static_cast<int>(t % a.n_tiles);
             if (m_pair != cur_m) {
                 cur_m = m_pair;
-                m = m_pair * 2 + rank;
-                my_row = m * kBM + q * 32 + lane;
-                my_valid = decompress_row_source(a, my_row, row_end) >= 0;
-                slab_full = __all_sync(0xffffffffu, my_valid);
+                const int64_t first = (m_pair * 2 + rank) * kBM + q * 32;
+                const int64_t my_row = first + lane;
+                const bool my_valid = decompress_row_source(a, my_row, row_end) >= 0;
+                row0 = a.k_buffer + first * a.n_out;
+                valid = __ballot_sync(0xffffffffu, my_valid);
 #pragma unroll
                 for (int kb = 0; kb < kKBMax; ++kb)
                     sa[kb] = (my_valid && kb < KB) ? x.q_scale[my_row * KB + kb] : 0.0f;
             }
+            float ws[kKBMax];  // this n tile's weight scales, loaded before the first wait
+#pragma unroll
+            for (int kb = 0; kb < kKBMax; ++kb)
+                ws[kb] = kb < KB ? __ldg(x.w_scale + static_cast<int64_t>(n) * KB + kb) : 0.0f;
             float acc[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
@@ -312,7 +317,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const float cs = sa[kb] * __ldg(x.w_scale + static_cast<int64_t>(n) * KB + kb);
+                const float cs = sa[kb] * ws[kb];
                 const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(kb) * kBN + h * 64;
                 uint32_t v0[32], v1[32];
@@ -332,31 +337,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t p[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) p[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
-            const int col = n * kBN + h * 64;
-            if (slab_full) {
-                if (lane == 0) bulk_wait_read<0>();  // the previous store read this box
-                __syncwarp();
-                const uint32_t rowaddr = smem_u32(stage) + lane * 128;
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    st_shared_v4(rowaddr + ((j ^ (lane & 7)) << 4), p[4 * j], p[4 * j + 1],
-                                 p[4 * j + 2], p[4 * j + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&tm_kbuf, stage, col, static_cast<int32_t>(m * kBM + q * 32));
-                    bulk_commit();
-                }
-            } else if (my_valid) {
-                uint16_t* dst = a.k_buffer + my_row * a.n_out + col;
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    st_v4(dst + j * 8, make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));
-            }
+            warp_store_rows_32x64(stage, p, row0 + n * kBN + h * 64, a.n_out, valid, lane);
             ++tile_i;
         }
-        if (lane == 0) bulk_wait<0>();
-        __syncwarp();
     }
 
     tc_fence_before();
@@ -380,7 +363,7 @@ cudaError_t launch_fp8_gather_quantize(DecompressArgs args, Fp8Extra extra, int 
 }
 
 cudaError_t launch_decompress_fp8_gemm(const CUtensorMap& tm_q, const CUtensorMap& tm_w,
-                                       const CUtensorMap& tm_kbuf, DecompressArgs args,
+                                       DecompressArgs args,
                                        Fp8Extra extra, int num_sms, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(decompress_fp8_gemm_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -389,7 +372,7 @@ cudaError_t launch_decompress_fp8_gemm(const CUtensorMap& tm_q, const CUtensorMa
     const int64_t max_pairs = num_sms / 2;
     const int64_t pairs = args.total_tiles < max_pairs ? args.total_tiles : max_pairs;
     decompress_fp8_gemm_kernel<<<static_cast<unsigned>(2 * pairs), kThreads, kSmemBytes, stream>>>(
-        tm_q, tm_w, tm_kbuf, args, extra);
+        tm_q, tm_w, args, extra);
     return cudaGetLastError();
 }
 

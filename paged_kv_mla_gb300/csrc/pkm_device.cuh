@@ -139,6 +139,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                  : "memory");
 }
 
+// Adds `bytes` to the transaction count of an mbarrier of either CTA of the cluster, without
+// arriving: the thread that will later arrive announces the bytes of a TMA load it issues.
+__device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t cluster_addr, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cluster.shared::cluster.b64 [%0], %1;" ::"r"(
+                     cluster_addr),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // Arrive on an mbarrier of either CTA of the cluster (shared::cluster address) with the
 // default release-at-CTA semantics.  Used for hand-offs whose data is ordered by tcgen05
 // fences (a TMEM accumulator drained by the epilogue), where a cluster-scope release would
@@ -229,6 +238,18 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         ".cta_group::2.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
+}
+
+// 4-D variant without an L2 policy (rows gathered from a paged cache, all k-blocks at once).
+__device__ __forceinline__ void tma_load_4d_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t c0, int32_t c1,
+                                                 int32_t c2, int32_t c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2 [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3)
         : "memory");
 }
 
@@ -351,6 +372,32 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                  : "r"(addr)
                  : "memory");
     return v;
+}
+
+// Stores a warp's 32-row x 64-column bf16 box to global memory in whole 128-byte row
+// segments.  On entry lane r holds row r as 32 packed bf16 pairs in `p`; the rows pass
+// through `stage` (4 KB of shared memory owned by the warp, 16-byte chunk j of row r kept
+// at chunk j ^ (r & 7), so both passes are free of bank conflicts) and come back out eight
+// lanes per row, so each store instruction writes four complete rows.  Row r goes to
+// row0 + r * pitch (elements) when bit r of `valid` is set.  This costs the warp a few
+// dozen instructions, where issuing a TMA store costs its thread several hundred cycles.
+__device__ __forceinline__ void warp_store_rows_32x64(uint32_t stage, const uint32_t (&p)[32],
+                                                      uint16_t* row0, int64_t pitch,
+                                                      uint32_t valid, int lane) {
+    const uint32_t rowaddr = stage + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        st_shared_v4(rowaddr + ((j ^ (lane & 7)) << 4), p[4 * j], p[4 * j + 1], p[4 * j + 2],
+                     p[4 * j + 3]);
+    __syncwarp();
+    const int chunk = lane & 7;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int r = it * 4 + (lane >> 3);
+        const uint4 v = ld_shared_v4(stage + r * 128 + ((chunk ^ (r & 7)) << 4));
+        if ((valid >> r) & 1u) st_v4(row0 + r * pitch + chunk * 8, v);
+    }
+    __syncwarp();  // the box may be overwritten once every lane has read its part
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

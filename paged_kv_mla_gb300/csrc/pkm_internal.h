@@ -34,6 +34,7 @@ struct DecompressArgs {
     int32_t n_tiles;               // N / bn
     int32_t m_tiles;               // ceil(L / rows per tile)
     int64_t total_tiles;           // m_tiles * n_tiles
+    int32_t gather_tma;            // bf16 kernel: the cache gather map is valid (page_size >= 8)
 };
 
 struct Fp8Extra {
@@ -64,12 +65,12 @@ struct KvMatmulArgs {
 
 // Launchers (return a CUDA error code; 0 = success).  Tensor maps are encoded by the
 // caller.
-cudaError_t launch_decompress_bf16(const CUtensorMap& tm_w, const CUtensorMap& tm_kbuf,
+cudaError_t launch_decompress_bf16(const CUtensorMap& tm_w, const CUtensorMap& tm_cache,
                                    DecompressArgs args, int num_sms, cudaStream_t stream);
 cudaError_t launch_fp8_gather_quantize(DecompressArgs args, Fp8Extra extra, int num_sms,
                                        cudaStream_t stream);
 cudaError_t launch_decompress_fp8_gemm(const CUtensorMap& tm_q, const CUtensorMap& tm_w,
-                                       const CUtensorMap& tm_kbuf, DecompressArgs args,
+                                       DecompressArgs args,
                                        Fp8Extra extra, int num_sms, cudaStream_t stream);
 cudaError_t launch_kv_matmul(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                              KvMatmulArgs args, int num_sms, cudaStream_t stream);
@@ -80,8 +81,9 @@ cudaError_t launch_wait_timeout_check(int32_t* status, uint64_t timeout_ns, cuda
 // -2 when the token resolves past the page-table row or to a page id >= num_pages.
 // The request of r is the largest b with row_offsets[b] <= r (row_offsets non-decreasing,
 // so empty requests are skipped); its token is cache_offsets[b] + r - row_offsets[b].
-__device__ __forceinline__ int64_t decompress_row_source(const DecompressArgs& a, int64_t r,
-                                                         int64_t row_end) {
+__device__ __forceinline__ int64_t decompress_row_locate(const DecompressArgs& a, int64_t r,
+                                                         int64_t row_end, uint32_t* page_out,
+                                                         uint32_t* slot_out) {
     if (r >= row_end) return -1;
     const uint32_t* bro = a.row_offsets;
     if (static_cast<uint64_t>(r) < static_cast<uint64_t>(__ldg(bro))) return -1;
@@ -97,8 +99,16 @@ __device__ __forceinline__ int64_t decompress_row_source(const DecompressArgs& a
     if (lp >= static_cast<uint64_t>(a.max_pages)) return -2;
     const uint32_t page = __ldg(a.page_table + static_cast<int64_t>(lo) * a.max_pages + lp);
     if (page >= static_cast<uint32_t>(a.num_pages)) return -2;
-    return static_cast<int64_t>(page) * a.page_stride +
-           static_cast<int64_t>(t % static_cast<uint64_t>(a.page_size)) * a.slot_stride;
+    const uint32_t slot = static_cast<uint32_t>(t % static_cast<uint64_t>(a.page_size));
+    *page_out = page;
+    *slot_out = slot;
+    return static_cast<int64_t>(page) * a.page_stride + static_cast<int64_t>(slot) * a.slot_stride;
+}
+
+__device__ __forceinline__ int64_t decompress_row_source(const DecompressArgs& a, int64_t r,
+                                                         int64_t row_end) {
+    uint32_t page, slot;
+    return decompress_row_locate(a, r, row_end, &page, &slot);
 }
 
 // min(buffer_length, row_offsets[batch]): rows at or past it are not written.
