@@ -159,14 +159,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t who = warp == 0 ? 0u : 1u;
             const uint64_t keep = policy_evict_last();
             uint32_t it = 0;
+            RingPos rp;
             bool issued[kStages] = {};
             uint32_t last_phase[kStages] = {};
             bool ok = true;
-            for (int64_t t = t_begin; t < t_end && ok; ++t) {
-                const int n = static_cast<int>(t % a.n_tiles);
-                for (int kb = 0; kb < KB; ++kb, ++it) {
+            for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid() && ok; w.next()) {
+                const int n = w.n;
+                for (int kb = 0; kb < KB; ++kb, ++it, rp.next(kStages)) {
                     if ((it & 1u) != who) continue;
-                    const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+                    const uint32_t s = rp.stage, ph = rp.phase;
                     if (!mbar_wait(&bars->b_empty[s], ph ^ 1, wc)) {
                         ok = false;
                         break;
@@ -193,11 +194,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---------------- MMA issuer (even CTA) ----------------
         if (leader && lane == 0) {
             const uint32_t idesc = idesc_bf16(256, bn, false, false);
-            uint32_t it = 0, tile_i = 0, seg = 0;
+            uint32_t tile_i = 0, seg = 0;
+            RingPos rp;
             int64_t cur_m = -1;
             bool ok = true;
-            for (int64_t t = t_begin; t < t_end && ok; ++t) {
-                const int64_t m = t / a.n_tiles;
+            for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid() && ok; w.next()) {
+                const int64_t m = w.m;
                 const bool new_seg = (m != cur_m);
                 if (new_seg) {
                     if (cur_m >= 0) {
@@ -212,7 +214,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint32_t d = tmem + acc * static_cast<uint32_t>(bn);
                 if (new_seg && !mbar_wait_cluster(&bars->a_full, seg & 1, wc)) break;
                 for (int kb = 0; kb < KB; ++kb) {
-                    const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+                    const uint32_t s = rp.stage, ph = rp.phase;
                     if (!mbar_wait(&bars->b_full[s], ph, wc)) {
                         ok = false;
                         break;
@@ -226,7 +228,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                       sdesc_sw128(b_addr + k * 32, 16, 1024), idesc,
                                       (kb | k) != 0 ? 1u : 0u);
                     mma_commit_pair(&bars->b_empty[s], 3);
-                    ++it;
+                    rp.next(kStages);
                 }
                 if (!ok) break;
                 mma_commit_pair(&bars->t_full[acc], 3);
@@ -247,11 +249,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t slot_units = static_cast<uint32_t>(a.slot_stride >> 3);
         const uint32_t a_full_leader = mapa_shared(smem_u32(&bars->a_full), 0);
         uint32_t seg = 0;
-        int64_t cur_m = -1;
-        for (int64_t t = t_begin; t < t_end; ++t) {
-            const int64_t m_pair = t / a.n_tiles;
-            if (m_pair == cur_m) continue;
-            cur_m = m_pair;
+        for (int64_t m_pair = t_begin / a.n_tiles; m_pair * a.n_tiles < t_end; ++m_pair) {
             const int64_t m = m_pair * 2 + rank;          // this CTA's 128-row block
             // the pair holding the block's middle tile copies its latent rows: it has at
             // least half the block's tiles left to hide the copy behind
@@ -341,9 +339,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int64_t cur_m = -1;
         uint16_t* row0 = a.k_buffer;  // first row of this warp's 32-row slab
         uint32_t valid = 0;           // bit r: slab row r is a buffer row with a source
-        for (int64_t t = t_begin; t < t_end; ++t) {
-            const int64_t m_pair = t / a.n_tiles;
-            const int n = static_cast<int>(t % a.n_tiles);
+        for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid(); w.next()) {
+            const int64_t m_pair = w.m;
+            const int n = w.n;
             if (m_pair != cur_m) {
                 cur_m = m_pair;
                 const int64_t first = (m_pair * 2 + rank) * kBM + q * 32;

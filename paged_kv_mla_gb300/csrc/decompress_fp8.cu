@@ -197,12 +197,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint64_t keep = policy_evict_last();
             const uint32_t a_full_leader = mapa_shared(smem_u32(&bars->a_full), 0);
-            uint32_t it = 0, seg = 0;
+            uint32_t seg = 0;
+            RingPos rp;
             int64_t cur_m = -1;
             bool ok = true;
-            for (int64_t t = t_begin; t < t_end && ok; ++t) {
-                const int64_t m_pair = t / a.n_tiles;
-                const int n = static_cast<int>(t % a.n_tiles);
+            for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid() && ok; w.next()) {
+                const int64_t m_pair = w.m;
+                const int n = w.n;
                 if (m_pair != cur_m) {
                     cur_m = m_pair;
                     if (seg > 0 && !mbar_wait(&bars->a_empty, (seg - 1) & 1, wc)) break;
@@ -215,7 +216,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     ++seg;
                 }
                 {  // one 3-D operation: all k-blocks of this CTA's 64 weight rows
-                    const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+                    const uint32_t s = rp.stage, ph = rp.phase;
                     if (!mbar_wait(&bars->b_empty[s], ph ^ 1, wc)) {
                         ok = false;
                         break;
@@ -226,7 +227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tma_load_3d_pair(sB + s * kBStageBytes, &tm_w,
                                      mapa_shared(smem_u32(&bars->b_full[s]), 0), 0,
                                      n * kBN + static_cast<int>(rank) * (kBN / 2), 0, keep);
-                    ++it;
+                    rp.next(kStages);
                 }
             }
             if (bars->abort_flag) spin_ns(50000);  // let loads in flight land before retiring
@@ -234,11 +235,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (leader && lane == 0) {
             const uint32_t idesc = idesc_e4m3(256, kBN);
-            uint32_t it = 0, tile_i = 0, seg = 0;
+            uint32_t tile_i = 0, seg = 0;
+            RingPos rp;
             int64_t cur_m = -1;
             bool ok = true;
-            for (int64_t t = t_begin; t < t_end && ok; ++t) {
-                const int64_t m = t / a.n_tiles;
+            for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid() && ok; w.next()) {
+                const int64_t m = w.m;
                 if (m != cur_m) {
                     if (cur_m >= 0) {
                         mma_commit_pair(&bars->a_empty, 3);
@@ -247,7 +249,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     cur_m = m;
                     if (!mbar_wait(&bars->a_full, seg & 1, wc)) break;
                 }
-                const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+                const uint32_t s = rp.stage, ph = rp.phase;
                 if (!mbar_wait(&bars->b_full[s], ph, wc)) break;
                 const uint32_t b_stage = smem_u32(sB + s * kBStageBytes);
                 for (int kb = 0; kb < KB; ++kb) {
@@ -267,7 +269,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     mma_commit_pair(&bars->t_full[kb], 3);
                 }
                 mma_commit_pair(&bars->b_empty[s], 3);
-                ++it;
+                rp.next(kStages);
                 ++tile_i;
             }
             mma_commit_pair(&bars->mma_done, 1);
@@ -287,9 +289,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t valid = 0;           // bit r: slab row r is a buffer row with a source
         float sa[kKBMax] = {0.f, 0.f, 0.f, 0.f};
         bool ok = true;
-        for (int64_t t = t_begin; t < t_end && ok; ++t) {
-            const int64_t m_pair = t / a.n_tiles;
-            const int n = static_cast<int>(t % a.n_tiles);
+        for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid() && ok; w.next()) {
+            const int64_t m_pair = w.m;
+            const int n = w.n;
             if (m_pair != cur_m) {
                 cur_m = m_pair;
                 const int64_t first = (m_pair * 2 + rank) * kBM + q * 32;

@@ -127,15 +127,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // (tens of MB) are kept in L2 ahead of the scattered cache writes
             const uint64_t keep = policy_evict_last();
             const uint32_t pair_tx = 2 * (kAStageBytes + static_cast<uint32_t>(half) * 128);
-            uint32_t it = 0;
+            RingPos rp;
             bool issued[kStages] = {};
             uint32_t last_phase[kStages] = {};
             bool ok = true;
-            for (int64_t t = t_begin; t < t_end && ok; ++t) {
-                const int64_t m = (t / a.n_tiles) * 2 + rank;  // this CTA's 128-row block
-                const int n = static_cast<int>(t % a.n_tiles);
+            for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid() && ok; w.next()) {
+                const int64_t m = w.m * 2 + rank;  // this CTA's 128-row block
+                const int n = w.n;
                 for (int kb = 0; kb < KB; ++kb) {
-                    const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+                    const uint32_t s = rp.stage, ph = rp.phase;
                     if (!mbar_wait(&bars->empty[s], ph ^ 1, wc)) {
                         ok = false;
                         break;
@@ -151,7 +151,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                          kb * 64, keep);
                     issued[s] = true;
                     last_phase[s] = ph;
-                    ++it;
+                    rp.next(kStages);
                 }
             }
             if (!ok) {
@@ -166,7 +166,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (leader && lane == 0) {
             const uint32_t idesc = idesc_bf16(256, bn, false, true);
-            uint32_t it = 0, tile_i = 0;
+            uint32_t tile_i = 0;
+            RingPos rp;
             bool ok = true;
             for (int64_t t = t_begin; t < t_end && ok; ++t) {
                 const uint32_t acc = tile_i & 1, aph = (tile_i >> 1) & 1;
@@ -174,7 +175,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d = tmem + acc * static_cast<uint32_t>(bn);
                 for (int kb = 0; kb < KB; ++kb) {
-                    const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+                    const uint32_t s = rp.stage, ph = rp.phase;
                     if (!mbar_wait(&bars->full[s], ph, wc)) {
                         ok = false;
                         break;
@@ -188,7 +189,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                       sdesc_sw128(b_addr + k * 2048, 8192, 1024), idesc,
                                       (kb | k) != 0 ? 1u : 0u);
                     mma_commit_pair(&bars->empty[s], 3);
-                    ++it;
+                    rp.next(kStages);
                 }
                 if (!ok) break;
                 mma_commit_pair(&bars->t_full[acc], 3);
@@ -204,9 +205,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t t_empty_leader = mapa_shared(smem_u32(&bars->t_empty[0]), 0);
         uint32_t tile_i = 0;
         int64_t cur_m = -1, my_dst = -1;
-        for (int64_t t = t_begin; t < t_end; ++t) {
-            const int64_t m = (t / a.n_tiles) * 2 + rank;
-            const int n = static_cast<int>(t % a.n_tiles);
+        for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid(); w.next()) {
+            const int64_t m = w.m * 2 + rank;
+            const int n = w.n;
             if (m != cur_m) {
                 cur_m = m;
                 my_dst = kv_row_dest(a, m * kBM + q * 32 + lane);

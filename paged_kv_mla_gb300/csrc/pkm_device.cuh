@@ -374,6 +374,36 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
+// Walks the tile ids [t_begin, t_end) of a persistent CTA (pair) as (m, n), n = t mod
+// n_tiles, with one division at the start instead of one per tile: the loops of the
+// MMA-issuing warp and of the warps sharing its scheduler stay short.
+struct TileWalk {
+    int64_t t, end, m;
+    int n, n_tiles;
+    __device__ __forceinline__ TileWalk(int64_t t_begin, int64_t t_end, int tiles)
+        : t(t_begin), end(t_end), m(t_begin / tiles),
+          n(static_cast<int>(t_begin % tiles)), n_tiles(tiles) {}
+    __device__ __forceinline__ bool valid() const { return t < end; }
+    __device__ __forceinline__ void next() {
+        ++t;
+        if (++n == n_tiles) {
+            n = 0;
+            ++m;
+        }
+    }
+};
+
+// Slot and phase parity of a ring of `stages` slots, advanced one slot at a time.
+struct RingPos {
+    uint32_t stage = 0, phase = 0;
+    __device__ __forceinline__ void next(uint32_t stages) {
+        if (++stage == stages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
 // Stores a warp's 32-row x 64-column bf16 box to global memory in whole 128-byte row
 // segments.  On entry lane r holds row r as 32 packed bf16 pairs in `p`; the rows pass
 // through `stage` (4 KB of shared memory owned by the warp, 16-byte chunk j of row r kept
