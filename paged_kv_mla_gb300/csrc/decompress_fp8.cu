@@ -329,10 +329,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_remote(t_empty_leader + kb * sizeof(uint64_t));
+                // packed FMAs: the two epilogue warps on the MMA warp's scheduler slow its
+                // MMA issue in proportion to the instructions they issue
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    acc[j] = fmaf(cs, __uint_as_float(v0[j]), acc[j]);
-                    acc[32 + j] = fmaf(cs, __uint_as_float(v1[j]), acc[32 + j]);
+                for (int j = 0; j < 32; j += 2) {
+                    fma2(acc[j], acc[j + 1], cs, __uint_as_float(v0[j]), __uint_as_float(v0[j + 1]));
+                    fma2(acc[32 + j], acc[33 + j], cs, __uint_as_float(v1[j]),
+                         __uint_as_float(v1[j + 1]));
                 }
             }
             if (!ok) break;

@@ -374,6 +374,19 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
+// d0 = a * b0 + d0 and d1 = a * b1 + d1, each rounded to nearest once (one packed
+// fma.rn.f32x2 instruction instead of two).
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %2};\n\t"
+        "mov.b64 rb, {%3, %4};\n\t"
+        "mov.b64 rc, {%0, %1};\n\t"
+        "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rc;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a), "f"(b0), "f"(b1));
+}
+
 // Walks the tile ids [t_begin, t_end) of a persistent CTA (pair) as (m, n), n = t mod
 // n_tiles, with one division at the start instead of one per tile: the loops of the
 // MMA-issuing warp and of the warps sharing its scheduler stay short.
