@@ -7,7 +7,8 @@ accumulation); this module compiles it with gcc and wraps it with numpy arrays.
 
 Each wrapper follows the passage cited in the C source:
   * generic_flare_mla_decompress_k_cache_ragged_paged -- description and Args
-  * mla_prefill_decode_graph_fp8 -- Parameters (scale granularities), Args (w_k, w_k_scale)
+  * mla_prefill_decode_graph_fp8 -- Parameters (scale granularities), Args (w_k, w_k_scale,
+    w_uv, w_uv_scale)
   * kv_matmul_ragged_paged -- Args (hidden_state, input_row_offsets, weight, kv_collection)
 """
 from __future__ import annotations
@@ -75,6 +76,23 @@ def lib():
             L.oracle_decompress_k_fp8_row.argtypes = cache_args + [_i32, _i32, _u8p, _f32p, _i32,
                                                                    _i64, _u16p, _u16p, _u8p, _f32p]
             L.oracle_decompress_k_fp8_row.restype = ctypes.c_int
+            L.oracle_up_project_v_bf16.argtypes = [_u16p, _i32, _u8p, _i32, _u16p, _i32, _i32, _i32,
+                                                    _u16p]
+            L.oracle_up_project_v_bf16.restype = None
+            L.oracle_decompress_kv.argtypes = cache_args + [_i32, _i32, _u16p, _i32, _u16p, _i32, _i32,
+                                                            _u16p, _u16p, _u16p, _u8p]
+            L.oracle_decompress_kv.restype = ctypes.c_int
+            L.oracle_decompress_kv_fp8.argtypes = cache_args + [_i32, _i32, _u8p, _f32p, _i32, _u8p,
+                                                                _f32p, _i32, _i32, _u16p, _u16p,
+                                                                _u16p, _u8p, _f32p, _u8p]
+            L.oracle_decompress_kv_fp8.restype = ctypes.c_int
+            L.oracle_decompress_kv_row.argtypes = cache_args + [_i32, _i32, _u16p, _i32, _u16p, _i32,
+                                                                _i32, _i64, _u16p, _u16p, _u16p]
+            L.oracle_decompress_kv_row.restype = ctypes.c_int
+            L.oracle_decompress_kv_fp8_row.argtypes = cache_args + [_i32, _i32, _u8p, _f32p, _i32,
+                                                                    _u8p, _f32p, _i32, _i32, _i64,
+                                                                    _u16p, _u16p, _u16p, _u8p, _f32p]
+            L.oracle_decompress_kv_fp8_row.restype = ctypes.c_int
             L.oracle_kv_matmul.argtypes = [_u16p, _u32p, _i32, _i32, _i32, _u16p, _i32, _u16p, _i64,
                                            _i64, _i64, _i64, _i32, _i32, _i32, _u32p, _i32, _u32p,
                                            _u32]
@@ -237,6 +255,108 @@ def decompress_k_fp8_row(cache: PagedCacheView, layer_idx, bro, co, batch, buffe
                                            _c(w_scale, np.float32).reshape(-1), n_out, int(r), lat,
                                            k, q, s)
     return st, lat, k, q, s
+
+
+def up_project_v_bf16(k_latent, latent_cols, w_uv, kv_lora_rank, row_written=None):
+    """V = latent x w_uv per head: w_uv [num_heads, v_head_dim, R]; returns [L, H, Dv]."""
+    k_latent = _c(k_latent, np.uint16)
+    w_uv = _c(w_uv, np.uint16)
+    L = k_latent.shape[0]
+    H, Dv = w_uv.shape[0], w_uv.shape[1]
+    out = np.zeros((L, H, Dv), np.uint16)
+    rw = np.ones(L, np.uint8) if row_written is None else _c(row_written, np.uint8)
+    lib().oracle_up_project_v_bf16(k_latent.reshape(-1), latent_cols, rw, L, w_uv.reshape(-1), H,
+                                   Dv, kv_lora_rank, out.reshape(-1))
+    return out
+
+
+def decompress_kv(cache: PagedCacheView, layer_idx, bro, co, batch, buffer_length, kv_lora_rank,
+                  rope_dim, w_k, w_uv, k_latent=None, k_buffer=None, v_buffer=None):
+    """bf16 K and V decompress (w_uv [H, Dv, R]).  Returns (status, k_latent, k_buffer,
+    v_buffer [L, H, Dv], row_written); pre-filled outputs are modified in place."""
+    w_k = _c(w_k, np.uint16)
+    w_uv = _c(w_uv, np.uint16)
+    n_out = w_k.shape[0]
+    H, Dv = w_uv.shape[0], w_uv.shape[1]
+    C = kv_lora_rank + rope_dim
+    L1 = max(buffer_length, 1)
+    if k_latent is None:
+        k_latent = np.zeros((L1, C), np.uint16)
+    if k_buffer is None:
+        k_buffer = np.zeros((L1, n_out), np.uint16)
+    if v_buffer is None:
+        v_buffer = np.zeros((L1, H, Dv), np.uint16)
+    written = np.zeros(L1, np.uint8)
+    st = lib().oracle_decompress_kv(*cache.args(layer_idx, bro, co, batch, buffer_length),
+                                    kv_lora_rank, rope_dim, w_k.reshape(-1), n_out,
+                                    w_uv.reshape(-1), H, Dv, k_latent.reshape(-1),
+                                    k_buffer.reshape(-1), v_buffer.reshape(-1), written)
+    return (st, k_latent[:buffer_length], k_buffer[:buffer_length], v_buffer[:buffer_length],
+            written[:buffer_length].astype(bool))
+
+
+def decompress_kv_fp8(cache: PagedCacheView, layer_idx, bro, co, batch, buffer_length,
+                      kv_lora_rank, rope_dim, w_e4m3, w_scale, w_uv_e4m3, w_uv_scale):
+    """FP8 K and V decompress.  Returns (status, k_latent, k_buffer, v_buffer, q_latent,
+    q_scale, row_written)."""
+    w_e4m3 = _c(w_e4m3, np.uint8)
+    w_uv_e4m3 = _c(w_uv_e4m3, np.uint8)
+    n_out = w_e4m3.shape[0]
+    H, Dv = w_uv_e4m3.shape[0], w_uv_e4m3.shape[1]
+    C = kv_lora_rank + rope_dim
+    L1 = max(buffer_length, 1)
+    k_latent = np.zeros((L1, C), np.uint16)
+    k_buffer = np.zeros((L1, n_out), np.uint16)
+    v_buffer = np.zeros((L1, H, Dv), np.uint16)
+    q = np.zeros((L1, kv_lora_rank), np.uint8)
+    qs = np.zeros((L1, kv_lora_rank // 128), np.float32)
+    written = np.zeros(L1, np.uint8)
+    st = lib().oracle_decompress_kv_fp8(*cache.args(layer_idx, bro, co, batch, buffer_length),
+                                        kv_lora_rank, rope_dim, w_e4m3.reshape(-1),
+                                        _c(w_scale, np.float32).reshape(-1), n_out,
+                                        w_uv_e4m3.reshape(-1), _c(w_uv_scale, np.float32).reshape(-1),
+                                        H, Dv, k_latent.reshape(-1), k_buffer.reshape(-1),
+                                        v_buffer.reshape(-1), q.reshape(-1), qs.reshape(-1), written)
+    return (st, k_latent[:buffer_length], k_buffer[:buffer_length], v_buffer[:buffer_length],
+            q[:buffer_length], qs[:buffer_length], written[:buffer_length].astype(bool))
+
+
+def decompress_kv_row(cache: PagedCacheView, layer_idx, bro, co, batch, buffer_length,
+                      kv_lora_rank, rope_dim, w_k, w_uv, r):
+    """One row of the bf16 K and V decompress.  Returns (status, latent_row, k_row, v_row)."""
+    w_k = _c(w_k, np.uint16)
+    w_uv = _c(w_uv, np.uint16)
+    n_out = w_k.shape[0]
+    H, Dv = w_uv.shape[0], w_uv.shape[1]
+    lat = np.zeros(kv_lora_rank + rope_dim, np.uint16)
+    k = np.zeros(n_out, np.uint16)
+    v = np.zeros(H * Dv, np.uint16)
+    st = lib().oracle_decompress_kv_row(*cache.args(layer_idx, bro, co, batch, buffer_length),
+                                        kv_lora_rank, rope_dim, w_k.reshape(-1), n_out,
+                                        w_uv.reshape(-1), H, Dv, int(r), lat, k, v)
+    return st, lat, k, v.reshape(H, Dv)
+
+
+def decompress_kv_fp8_row(cache: PagedCacheView, layer_idx, bro, co, batch, buffer_length,
+                          kv_lora_rank, rope_dim, w_e4m3, w_scale, w_uv_e4m3, w_uv_scale, r):
+    """One row of the FP8 K and V decompress.  Returns (status, latent_row, k_row, v_row,
+    q_row, scale_row)."""
+    w_e4m3 = _c(w_e4m3, np.uint8)
+    w_uv_e4m3 = _c(w_uv_e4m3, np.uint8)
+    n_out = w_e4m3.shape[0]
+    H, Dv = w_uv_e4m3.shape[0], w_uv_e4m3.shape[1]
+    lat = np.zeros(kv_lora_rank + rope_dim, np.uint16)
+    k = np.zeros(n_out, np.uint16)
+    v = np.zeros(H * Dv, np.uint16)
+    q = np.zeros(kv_lora_rank, np.uint8)
+    s = np.zeros(kv_lora_rank // 128, np.float32)
+    st = lib().oracle_decompress_kv_fp8_row(*cache.args(layer_idx, bro, co, batch, buffer_length),
+                                            kv_lora_rank, rope_dim, w_e4m3.reshape(-1),
+                                            _c(w_scale, np.float32).reshape(-1), n_out,
+                                            w_uv_e4m3.reshape(-1),
+                                            _c(w_uv_scale, np.float32).reshape(-1), H, Dv, int(r),
+                                            lat, k, v, q, s)
+    return st, lat, k, v.reshape(H, Dv), q, s
 
 
 def kv_matmul(hidden_state, input_row_offsets, batch, total_rows, weight, cache: PagedCacheView,

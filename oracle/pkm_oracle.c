@@ -16,6 +16,8 @@
  *     buffer_row_offsets, cache_offsets, buffer_length): the same decompress with an
  *     e4m3 weight carrying block scales; the activations are quantised per token per
  *     128-column block (the reading of the silent points is stated at each function).
+ *   - mla_prefill_decode_graph_fp8, Args w_uv / w_uv_scale: the V up-projection of the same
+ *     gathered latent rows (bf16 and block-scaled FP8).
  *   - kv_matmul_ragged_paged (Modular MAX kernels, nn/kv_cache_ragged), Args: a GEMM on
  *     the ragged hidden_state whose rows are written into the paged cache of one layer,
  *     after each request's existing cache length.
@@ -378,6 +380,172 @@ int oracle_decompress_k_fp8_row(const uint16_t* cache, int64_t layer_stride,
         }
     }
     return 1;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* V up-projection with w_uv (mla_prefill_decode_graph_fp8, Args w_uv / w_uv_scale)      */
+/* ------------------------------------------------------------------------------------ */
+
+/*
+ * w_uv is the "weight tensor for projecting latent values to V", shape [num_heads,
+ * v_head_dim, kv_latent_dim].  For every written row r (the rows step 1 of the
+ * decompress gathered), head h and d < v_head_dim:
+ *   v[r, h, d] = bf16_rne( sum_{k < R} latent[r, k] * w_uv[h, d, k] ),
+ * summed in fp64 in order of k, over the first R = kv_lora_rank latent columns (the
+ * latent "values" are the same gathered rows the K up-projection reads; the rope columns
+ * take no part).  v_buffer is [buffer_length, num_heads, v_head_dim] row-major.
+ */
+void oracle_up_project_v_bf16(const uint16_t* k_latent, int32_t latent_cols,
+                              const uint8_t* row_written, int32_t buffer_length,
+                              const uint16_t* w_uv, int32_t num_heads, int32_t v_head_dim,
+                              int32_t kv_lora_rank, uint16_t* v_buffer) {
+    for (int64_t r = 0; r < buffer_length; ++r) {
+        if (row_written && !row_written[r]) continue;
+        const uint16_t* a = k_latent + r * latent_cols;
+        for (int64_t h = 0; h < num_heads; ++h) {
+            for (int64_t d = 0; d < v_head_dim; ++d) {
+                const uint16_t* w = w_uv + (h * v_head_dim + d) * kv_lora_rank;
+                double acc = 0.0;
+                for (int64_t k = 0; k < kv_lora_rank; ++k)
+                    acc += oracle_bf16_to_double(a[k]) * oracle_bf16_to_double(w[k]);
+                v_buffer[(r * num_heads + h) * v_head_dim + d] = oracle_double_to_bf16(acc);
+            }
+        }
+    }
+}
+
+/*
+ * K and V from one gather: step 1 (gather), step 2 with w_k into k_buffer, and the V
+ * up-projection with w_uv into v_buffer.  Returns the gather's status.
+ */
+int oracle_decompress_kv(const uint16_t* cache, int64_t layer_stride, int64_t page_stride,
+                         int64_t slot_stride, int32_t num_pages, int32_t page_size,
+                         const uint32_t* page_table, int32_t max_pages_per_seq,
+                         uint32_t layer_idx, const uint32_t* buffer_row_offsets,
+                         const uint32_t* cache_offsets, int32_t batch, int32_t buffer_length,
+                         int32_t kv_lora_rank, int32_t rope_dim, const uint16_t* w_k,
+                         int32_t n_out, const uint16_t* w_uv, int32_t num_heads,
+                         int32_t v_head_dim, uint16_t* k_latent, uint16_t* k_buffer,
+                         uint16_t* v_buffer, uint8_t* row_written) {
+    int32_t latent_cols = kv_lora_rank + rope_dim;
+    int st = oracle_gather_latent(cache, layer_stride, page_stride, slot_stride, num_pages,
+                                  page_size, page_table, max_pages_per_seq, layer_idx,
+                                  buffer_row_offsets, cache_offsets, batch, buffer_length,
+                                  latent_cols, k_latent, row_written);
+    oracle_up_project_bf16(k_latent, latent_cols, row_written, buffer_length, w_k,
+                           kv_lora_rank, n_out, k_buffer);
+    oracle_up_project_v_bf16(k_latent, latent_cols, row_written, buffer_length, w_uv,
+                             num_heads, v_head_dim, kv_lora_rank, v_buffer);
+    return st;
+}
+
+/*
+ * Block-scaled V product of one quantised row with the e4m3 w_uv.  Reading of the silent
+ * point: w_uv_scale has the same 128 x 128 block granularity as w_k_scale over w_uv seen
+ * as a [num_heads * v_head_dim, R] matrix, i.e. w_uv_scale[(h * v_head_dim + d) / 128,
+ * k / 128]:
+ *   v[h, d] = bf16_rne( sum_kb sa[kb] * sv[(h*Dv + d)/128, kb]
+ *                        * sum_{k in kb} dq(q[k]) * dq(w_uv[h, d, k]) )  in fp64.
+ */
+static void fp8_row_product_v(const uint8_t* q_row, const float* sa_row, const uint8_t* qv,
+                              const float* sv, int32_t num_heads, int32_t v_head_dim,
+                              int32_t kv_lora_rank, uint16_t* v_row) {
+    int32_t kblocks = kv_lora_rank / 128;
+    for (int64_t h = 0; h < num_heads; ++h) {
+        for (int64_t d = 0; d < v_head_dim; ++d) {
+            const int64_t j = h * v_head_dim + d;
+            double total = 0.0;
+            for (int32_t kb = 0; kb < kblocks; ++kb) {
+                double part = 0.0;
+                for (int64_t k = (int64_t)kb * 128; k < (int64_t)kb * 128 + 128; ++k)
+                    part += oracle_e4m3_to_double(q_row[k]) *
+                            oracle_e4m3_to_double(qv[j * kv_lora_rank + k]);
+                total += (double)sa_row[kb] * (double)sv[(j / 128) * kblocks + kb] * part;
+            }
+            v_row[j] = oracle_double_to_bf16(total);
+        }
+    }
+}
+
+/*
+ * FP8 K and V from one gather and one activation quantisation: the rows are gathered and
+ * quantised exactly as in oracle_decompress_k_fp8, then multiplied by w_k (into
+ * k_buffer) and by w_uv (into v_buffer [buffer_length, num_heads, v_head_dim]).
+ */
+int oracle_decompress_kv_fp8(const uint16_t* cache, int64_t layer_stride, int64_t page_stride,
+                             int64_t slot_stride, int32_t num_pages, int32_t page_size,
+                             const uint32_t* page_table, int32_t max_pages_per_seq,
+                             uint32_t layer_idx, const uint32_t* buffer_row_offsets,
+                             const uint32_t* cache_offsets, int32_t batch,
+                             int32_t buffer_length, int32_t kv_lora_rank, int32_t rope_dim,
+                             const uint8_t* w_e4m3, const float* w_scale, int32_t n_out,
+                             const uint8_t* w_uv_e4m3, const float* w_uv_scale,
+                             int32_t num_heads, int32_t v_head_dim, uint16_t* k_latent,
+                             uint16_t* k_buffer, uint16_t* v_buffer, uint8_t* q_latent,
+                             float* q_scale, uint8_t* row_written) {
+    int st = oracle_decompress_k_fp8(cache, layer_stride, page_stride, slot_stride, num_pages,
+                                     page_size, page_table, max_pages_per_seq, layer_idx,
+                                     buffer_row_offsets, cache_offsets, batch, buffer_length,
+                                     kv_lora_rank, rope_dim, w_e4m3, w_scale, n_out, k_latent,
+                                     k_buffer, q_latent, q_scale, row_written);
+    int32_t kblocks = kv_lora_rank / 128;
+    int64_t nv = (int64_t)num_heads * v_head_dim;
+    for (int64_t r = 0; r < buffer_length; ++r) {
+        if (!row_written[r]) continue;
+        fp8_row_product_v(q_latent + r * kv_lora_rank, q_scale + r * kblocks, w_uv_e4m3,
+                          w_uv_scale, num_heads, v_head_dim, kv_lora_rank, v_buffer + r * nv);
+    }
+    return st;
+}
+
+/*
+ * Single-row forms for sampled checks at full size (same return codes as
+ * oracle_decompress_k_row).  The FP8 form also returns the quantised row.
+ */
+int oracle_decompress_kv_row(const uint16_t* cache, int64_t layer_stride,
+                             int64_t page_stride, int64_t slot_stride, int32_t num_pages,
+                             int32_t page_size, const uint32_t* page_table,
+                             int32_t max_pages_per_seq, uint32_t layer_idx,
+                             const uint32_t* buffer_row_offsets,
+                             const uint32_t* cache_offsets, int32_t batch,
+                             int32_t buffer_length, int32_t kv_lora_rank, int32_t rope_dim,
+                             const uint16_t* w_k, int32_t n_out, const uint16_t* w_uv,
+                             int32_t num_heads, int32_t v_head_dim, int64_t r,
+                             uint16_t* latent_row, uint16_t* k_row, uint16_t* v_row) {
+    int st = oracle_decompress_k_row(cache, layer_stride, page_stride, slot_stride, num_pages,
+                                     page_size, page_table, max_pages_per_seq, layer_idx,
+                                     buffer_row_offsets, cache_offsets, batch, buffer_length,
+                                     kv_lora_rank, rope_dim, w_k, n_out, r, latent_row, k_row);
+    if (st != 0) return st;
+    const uint8_t one = 1;
+    oracle_up_project_v_bf16(latent_row, kv_lora_rank + rope_dim, &one, 1, w_uv, num_heads,
+                             v_head_dim, kv_lora_rank, v_row);
+    return 0;
+}
+
+int oracle_decompress_kv_fp8_row(const uint16_t* cache, int64_t layer_stride,
+                                 int64_t page_stride, int64_t slot_stride, int32_t num_pages,
+                                 int32_t page_size, const uint32_t* page_table,
+                                 int32_t max_pages_per_seq, uint32_t layer_idx,
+                                 const uint32_t* buffer_row_offsets,
+                                 const uint32_t* cache_offsets, int32_t batch,
+                                 int32_t buffer_length, int32_t kv_lora_rank,
+                                 int32_t rope_dim, const uint8_t* w_e4m3,
+                                 const float* w_scale, int32_t n_out,
+                                 const uint8_t* w_uv_e4m3, const float* w_uv_scale,
+                                 int32_t num_heads, int32_t v_head_dim, int64_t r,
+                                 uint16_t* latent_row, uint16_t* k_row, uint16_t* v_row,
+                                 uint8_t* q_row, float* scale_row) {
+    int st = oracle_decompress_k_fp8_row(cache, layer_stride, page_stride, slot_stride,
+                                         num_pages, page_size, page_table, max_pages_per_seq,
+                                         layer_idx, buffer_row_offsets, cache_offsets, batch,
+                                         buffer_length, kv_lora_rank, rope_dim, w_e4m3,
+                                         w_scale, n_out, r, latent_row, k_row, q_row,
+                                         scale_row);
+    if (st != 0) return st;
+    fp8_row_product_v(q_row, scale_row, w_uv_e4m3, w_uv_scale, num_heads, v_head_dim,
+                      kv_lora_rank, v_row);
+    return 0;
 }
 
 /* ------------------------------------------------------------------------------------ */

@@ -88,6 +88,9 @@ class DecompressInputs:
     w_k: Optional[np.ndarray] = None        # uint16 bf16 [n_out, kv_lora_rank]
     w_k_e4m3: Optional[np.ndarray] = None   # uint8 [n_out, kv_lora_rank]
     w_k_scale: Optional[np.ndarray] = None  # float32 [n_out/128, kv_lora_rank/128]
+    w_uv: Optional[np.ndarray] = None       # uint16 bf16 [num_heads, v_head_dim, kv_lora_rank]
+    w_uv_e4m3: Optional[np.ndarray] = None  # uint8 [num_heads, v_head_dim, kv_lora_rank]
+    w_uv_scale: Optional[np.ndarray] = None  # float32 [num_heads*v_head_dim/128, kv_lora_rank/128]
     lengths: Optional[np.ndarray] = None
     meta: dict = field(default_factory=dict)
 
@@ -180,6 +183,34 @@ def make_decompress(name, seed, lengths, cache_offsets, page_size, kv_lora_rank,
     else:
         d.w_k = bf16_normal((n_out, kv_lora_rank), std, g)
     return d
+
+
+def add_v_weight(d: DecompressInputs, num_heads, v_head_dim, seed, w_std=None, fp8=False,
+                 int_values=False) -> DecompressInputs:
+    """Adds a w_uv [num_heads, v_head_dim, kv_lora_rank] drawn from its own seeded generator
+    (bf16 ~N(0, std^2), or e4m3 codes + 128x128 block scales quantised like W_k, or small
+    integers), so the rest of the problem is the same as without it."""
+    g = _gen(seed)
+    R = d.kv_lora_rank
+    std = w_std if w_std is not None else 1.0 / math.sqrt(R)
+    if fp8:
+        w = torch.randn(num_heads * v_head_dim, R, generator=g, dtype=torch.float32) * std
+        q, sc = quantize_weight_e4m3(w)
+        d.w_uv_e4m3 = q.reshape(num_heads, v_head_dim, R)
+        d.w_uv_scale = sc
+    elif int_values:
+        d.w_uv = bf16_small_ints((num_heads, v_head_dim, R), -2, 2, g)
+    else:
+        d.w_uv = bf16_normal((num_heads, v_head_dim, R), std, g)
+    return d
+
+
+def deepseek_decompress_kv(seed=1001, fp8=False) -> DecompressInputs:
+    """The DeepSeek-V3-shaped decompress with the V up-projection as well: w_uv [128 heads,
+    v_head_dim 128, 512] ~N(0, 1/512) (bf16, or e4m3 with 128x128 block scales), seed 1006."""
+    d = deepseek_decompress(seed, fp8=fp8)
+    d.name = d.name + "_kv"
+    return add_v_weight(d, 128, 128, 1006, fp8=fp8)
 
 
 def tiny_decompress(seed=1000) -> DecompressInputs:
@@ -313,5 +344,7 @@ WORKLOADS = {
     "deepseek_v3_bf16_decompress": lambda: deepseek_decompress(1001, fp8=False),
     "deepseek_v3_fp8_decompress": lambda: deepseek_decompress(1001, fp8=True),
     "long_context_decompress": long_context_decompress,
+    "deepseek_v3_bf16_decompress_kv": lambda: deepseek_decompress_kv(1001, fp8=False),
+    "deepseek_v3_fp8_decompress_kv": lambda: deepseek_decompress_kv(1001, fp8=True),
     "kv_matmul_write_path": kv_matmul_write_path,
 }
