@@ -135,6 +135,33 @@ pkm_status mla_decompress_k_paged(const pkm_paged_cache* cache, uint32_t layer_i
                                   void* stream);
 
 /*
+ * bf16 latent-K and V decompress: one gather for both up-projections.
+ * Source: generic_flare_mla_decompress_k_cache_ragged_paged (the gather and K, as for
+ * mla_decompress_k_paged) and mla_prefill_decode_graph_fp8 -- Args w_uv ("Weight tensor
+ * for projecting latent values to V. Shape: [num_heads, v_head_dim, kv_latent_dim]").
+ *
+ * Computes exactly what mla_decompress_k_paged computes (k_latent_buffer, k_buffer) and,
+ * for every written row r, head h and d < v_head_dim:
+ *     v_buffer[r, h, d] = bf16( sum_{k < kv_lora_rank} k_latent_buffer[r, k] * w_uv[h, d, k] )
+ * (fp32 accumulation, round to nearest even).  Rows of v_buffer that no request covers
+ * are left untouched, like those of the other outputs.
+ *
+ *   w_uv                 device bf16 [num_heads, v_head_dim, kv_lora_rank], 16-byte aligned.
+ *   num_heads, v_head_dim  > 0, num_heads * v_head_dim a multiple of 64.
+ *   v_buffer             device bf16 [buffer_length, num_heads, v_head_dim], row-major,
+ *                        16-byte aligned.
+ *   other arguments      as for mla_decompress_k_paged (same errors).
+ */
+pkm_status mla_decompress_kv_paged(const pkm_paged_cache* cache, uint32_t layer_idx,
+                                   const uint32_t* buffer_row_offsets,
+                                   const uint32_t* cache_offsets, int32_t batch,
+                                   int32_t buffer_length, int32_t kv_lora_rank,
+                                   int32_t rope_dim, const void* w_k, int32_t n_out,
+                                   const void* w_uv, int32_t num_heads, int32_t v_head_dim,
+                                   void* k_latent_buffer, void* k_buffer, void* v_buffer,
+                                   int32_t* dev_status, void* stream);
+
+/*
  * Bytes of device workspace mla_decompress_k_paged_fp8 needs for buffer_length rows of
  * kv_lora_rank latent columns (0 for invalid sizes).  Layout, for a caller that wants to
  * read the quantised activations back:
@@ -176,6 +203,38 @@ pkm_status mla_decompress_k_paged_fp8(const pkm_paged_cache* cache, uint32_t lay
                                       void* k_latent_buffer, void* k_buffer, void* workspace,
                                       size_t workspace_bytes, int32_t* dev_status,
                                       void* stream);
+
+/*
+ * FP8 block-scaled latent-K and V decompress: one gather and one activation quantisation
+ * for both up-projections.
+ * Source: mla_prefill_decode_graph_fp8 -- Args w_k, w_k_scale, w_uv ("Weight tensor for
+ * projecting latent values to V", [num_heads, v_head_dim, kv_latent_dim]), w_uv_scale
+ * ("Scale tensor for w_uv").
+ *
+ * Computes exactly what mla_decompress_k_paged_fp8 computes (k_latent_buffer, k_buffer,
+ * the workspace) and, with the same quantised row q[r, :] and scales s[r, kb]:
+ *     v_buffer[r, h, d] = bf16( sum_kb s[r, kb] * w_uv_scale[j/128, kb]
+ *                               * sum_{k in kb} q[r, k] * w_uv_e4m3[h, d, k] ),  j = h*v_head_dim + d
+ * i.e. w_uv_scale has w_k_scale's 128 x 128 granularity over w_uv read as a
+ * [num_heads * v_head_dim, kv_lora_rank] matrix (the page gives no layout for it).
+ *
+ *   w_uv_e4m3            device e4m3 [num_heads, v_head_dim, kv_lora_rank], 16-byte aligned.
+ *   w_uv_scale           device fp32 [num_heads*v_head_dim/128, kv_lora_rank/128].
+ *   num_heads, v_head_dim  > 0, num_heads * v_head_dim a multiple of 128.
+ *   v_buffer             device bf16 [buffer_length, num_heads, v_head_dim], 16-byte aligned.
+ *   other arguments      as for mla_decompress_k_paged_fp8 (same workspace size).
+ */
+pkm_status mla_decompress_kv_paged_fp8(const pkm_paged_cache* cache, uint32_t layer_idx,
+                                       const uint32_t* buffer_row_offsets,
+                                       const uint32_t* cache_offsets, int32_t batch,
+                                       int32_t buffer_length, int32_t kv_lora_rank,
+                                       int32_t rope_dim, const void* w_k_e4m3,
+                                       const float* w_k_scale, int32_t n_out,
+                                       const void* w_uv_e4m3, const float* w_uv_scale,
+                                       int32_t num_heads, int32_t v_head_dim,
+                                       void* k_latent_buffer, void* k_buffer, void* v_buffer,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t* dev_status, void* stream);
 
 /*
  * FP8 decompress for callers that cannot allocate device memory.  The paper has no

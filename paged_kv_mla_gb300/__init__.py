@@ -64,6 +64,13 @@ _lib.mla_decompress_k_paged_fp8.argtypes = [ctypes.POINTER(_CCache), _u32, _vp, 
                                             _i32, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp,
                                             _vp]
 _lib.mla_decompress_k_paged_fp8.restype = ctypes.c_int
+_lib.mla_decompress_kv_paged.argtypes = [ctypes.POINTER(_CCache), _u32, _vp, _vp, _i32, _i32, _i32,
+                                         _i32, _vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
+_lib.mla_decompress_kv_paged.restype = ctypes.c_int
+_lib.mla_decompress_kv_paged_fp8.argtypes = [ctypes.POINTER(_CCache), _u32, _vp, _vp, _i32, _i32,
+                                             _i32, _i32, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _vp,
+                                             _vp, _vp, _vp, _sz, _vp, _vp]
+_lib.mla_decompress_kv_paged_fp8.restype = ctypes.c_int
 _lib.kv_matmul_paged.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _i32, ctypes.POINTER(_CCache),
                                  _u32, _vp, _vp]
 _lib.kv_matmul_paged.restype = ctypes.c_int
@@ -145,6 +152,24 @@ def mla_decompress_k_paged(cache: PagedCache, layer_idx: int, buffer_row_offsets
     return _check(code, "mla_decompress_k_paged", check)
 
 
+def mla_decompress_kv_paged(cache: PagedCache, layer_idx: int, buffer_row_offsets: torch.Tensor,
+                            cache_offsets: torch.Tensor, buffer_length: int, kv_lora_rank: int,
+                            rope_dim: int, w_k: torch.Tensor, w_uv: torch.Tensor,
+                            k_latent_buffer: torch.Tensor, k_buffer: torch.Tensor,
+                            v_buffer: torch.Tensor, dev_status: Optional[torch.Tensor] = None,
+                            stream=None, check: bool = True) -> int:
+    """K and V from one gather; w_uv is [num_heads, v_head_dim, kv_lora_rank]."""
+    c = cache.c_struct()
+    batch = int(buffer_row_offsets.shape[0]) - 1
+    code = _lib.mla_decompress_kv_paged(ctypes.byref(c), int(layer_idx), _ptr(buffer_row_offsets),
+                                        _ptr(cache_offsets), batch, int(buffer_length),
+                                        int(kv_lora_rank), int(rope_dim), _ptr(w_k),
+                                        int(w_k.shape[0]), _ptr(w_uv), int(w_uv.shape[0]),
+                                        int(w_uv.shape[1]), _ptr(k_latent_buffer), _ptr(k_buffer),
+                                        _ptr(v_buffer), _ptr(dev_status), _stream(stream))
+    return _check(code, "mla_decompress_kv_paged", check)
+
+
 def mla_decompress_k_paged_fp8_workspace_size(buffer_length: int, kv_lora_rank: int) -> int:
     return int(_lib.mla_decompress_k_paged_fp8_workspace_size(int(buffer_length), int(kv_lora_rank)))
 
@@ -173,6 +198,28 @@ def mla_decompress_k_paged_fp8(cache: PagedCache, layer_idx: int,
         int(w_k_e4m3.shape[0]), _ptr(k_latent_buffer), _ptr(k_buffer), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
     return _check(code, "mla_decompress_k_paged_fp8", check)
+
+
+def mla_decompress_kv_paged_fp8(cache: PagedCache, layer_idx: int,
+                                buffer_row_offsets: torch.Tensor, cache_offsets: torch.Tensor,
+                                buffer_length: int, kv_lora_rank: int, rope_dim: int,
+                                w_k_e4m3: torch.Tensor, w_k_scale: torch.Tensor,
+                                w_uv_e4m3: torch.Tensor, w_uv_scale: torch.Tensor,
+                                k_latent_buffer: torch.Tensor, k_buffer: torch.Tensor,
+                                v_buffer: torch.Tensor, workspace: torch.Tensor,
+                                dev_status: Optional[torch.Tensor] = None, stream=None,
+                                check: bool = True) -> int:
+    """FP8 K and V from one gather and one activation quantisation."""
+    c = cache.c_struct()
+    batch = int(buffer_row_offsets.shape[0]) - 1
+    code = _lib.mla_decompress_kv_paged_fp8(
+        ctypes.byref(c), int(layer_idx), _ptr(buffer_row_offsets), _ptr(cache_offsets), batch,
+        int(buffer_length), int(kv_lora_rank), int(rope_dim), _ptr(w_k_e4m3), _ptr(w_k_scale),
+        int(w_k_e4m3.shape[0]), _ptr(w_uv_e4m3), _ptr(w_uv_scale), int(w_uv_e4m3.shape[0]),
+        int(w_uv_e4m3.shape[1]), _ptr(k_latent_buffer), _ptr(k_buffer), _ptr(v_buffer),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
+        _stream(stream))
+    return _check(code, "mla_decompress_kv_paged_fp8", check)
 
 
 def mla_decompress_k_paged_fp8_noalloc(cache: PagedCache, layer_idx: int,

@@ -205,12 +205,35 @@ const char* pkm_status_string(pkm_status status) {
     return "PKM_ERR_UNKNOWN";
 }
 
-pkm_status mla_decompress_k_paged(const pkm_paged_cache* cache, uint32_t layer_idx,
-                                  const uint32_t* buffer_row_offsets,
-                                  const uint32_t* cache_offsets, int32_t batch,
-                                  int32_t buffer_length, int32_t kv_lora_rank, int32_t rope_dim,
-                                  const void* w_k, int32_t n_out, void* k_latent_buffer,
-                                  void* k_buffer, int32_t* dev_status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// V operands of the K-and-V entry points (all null / zero for the K-only ones).
+struct VOperands {
+    const void* w_uv = nullptr;   // [num_heads, v_head_dim, R], bf16 or e4m3
+    const float* w_uv_scale = nullptr;
+    int32_t n_v = 0;              // num_heads * v_head_dim
+    void* v_buffer = nullptr;     // [buffer_length, n_v] bf16
+};
+
+pkm_status check_v(const VOperands& v, int32_t num_heads, int32_t v_head_dim, int multiple) {
+    if (v.w_uv == nullptr || v.v_buffer == nullptr) return PKM_ERR_INVALID_ARG;
+    if (num_heads <= 0 || v_head_dim <= 0) return PKM_ERR_INVALID_ARG;
+    if (!aligned16(v.w_uv) || !aligned16(v.v_buffer)) return PKM_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(num_heads) * v_head_dim > (static_cast<int64_t>(1) << 30))
+        return PKM_ERR_UNSUPPORTED;
+    if ((static_cast<int64_t>(num_heads) * v_head_dim) % multiple != 0) return PKM_ERR_UNSUPPORTED;
+    return PKM_OK;
+}
+
+// Body of the bf16 entry points: K alone (v.w_uv == nullptr) or K and V from one gather.
+pkm_status decompress_bf16(const pkm_paged_cache* cache, uint32_t layer_idx,
+                           const uint32_t* buffer_row_offsets, const uint32_t* cache_offsets,
+                           int32_t batch, int32_t buffer_length, int32_t kv_lora_rank,
+                           int32_t rope_dim, const void* w_k, int32_t n_out,
+                           const VOperands& v, void* k_latent_buffer, void* k_buffer,
+                           int32_t* dev_status, void* stream) {
     bool empty = false;
     pkm_status st = check_decompress_sizes(batch, buffer_length, kv_lora_rank, rope_dim, n_out,
                                            &empty);
@@ -225,20 +248,36 @@ pkm_status mla_decompress_k_paged(const pkm_paged_cache* cache, uint32_t layer_i
                                static_cast<int64_t>(cache->page_size) * cache->slot_stride;
     if (layer_span >= (static_cast<int64_t>(1) << 35) - 64) return PKM_ERR_UNSUPPORTED;
     // CTA-pair tiles of 256 rows x bn columns (the widest of 256 / 128 / 64 dividing
-    // n_out); each CTA loads bn/2 W_k rows per k-block
-    const int bn = (n_out % 256 == 0) ? 256 : (n_out % 128 == 0) ? 128 : 64;
+    // n_out, and n_v with V); each CTA loads bn/2 weight rows per k-block
+    const int32_t nv = v.w_uv != nullptr ? v.n_v : 0;
+    const int32_t both = nv > 0 ? (n_out | nv) : n_out;
+    const int bn = (both % 256 == 0) ? 256 : (both % 128 == 0) ? 128 : 64;
     DecompressArgs a = make_decompress_args(cache, layer_idx, buffer_row_offsets, cache_offsets,
                                             batch, buffer_length, kv_lora_rank, rope_dim, n_out,
                                             k_latent_buffer, k_buffer, dev_status, bn);
+    a.n_tiles_k = a.n_tiles;
+    if (nv > 0) {
+        a.v_buffer = static_cast<uint16_t*>(v.v_buffer);
+        a.n_out_v = nv;
+        a.n_tiles += nv / bn;
+    }
     int sms = 0;
     if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
     a.m_tiles = (buffer_length + 255) / 256;
     a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
     alignas(64) CUtensorMap tm_w;
+    alignas(64) CUtensorMap tm_wv;
     alignas(64) CUtensorMap tm_c = {};
     if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_k, kv_lora_rank, n_out,
                    static_cast<uint64_t>(kv_lora_rank) * 2, 64, bn / 2))
         return PKM_ERR_CUDA;
+    if (nv > 0) {
+        if (!encode_2d(&tm_wv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v.w_uv, kv_lora_rank, nv,
+                       static_cast<uint64_t>(kv_lora_rank) * 2, 64, bn / 2))
+            return PKM_ERR_CUDA;
+    } else {
+        tm_wv = tm_w;
+    }
     // Rows arriving as runs of eight slots of one page come by TMA; that needs pages of at
     // least eight slots.  Otherwise every row takes the per-row path.
     a.gather_tma = cache->page_size >= 8 ? 1 : 0;
@@ -246,10 +285,112 @@ pkm_status mla_decompress_k_paged(const pkm_paged_cache* cache, uint32_t layer_i
         !encode_cache_gather(&tm_c, a.cache_layer, cache->page_size, cache->num_pages,
                              kv_lora_rank / 64, cache->slot_stride, cache->page_stride))
         return PKM_ERR_CUDA;
-    return pkm::launch_decompress_bf16(tm_w, tm_c, a, sms, static_cast<cudaStream_t>(stream)) ==
-                   cudaSuccess
+    return pkm::launch_decompress_bf16(tm_w, tm_wv, tm_c, a, sms,
+                                       static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PKM_OK
                : PKM_ERR_CUDA;
+}
+
+// Body of the FP8 entry points: K alone (v.w_uv == nullptr) or K and V, the activations
+// quantised once for both.
+pkm_status decompress_fp8(const pkm_paged_cache* cache, uint32_t layer_idx,
+                          const uint32_t* buffer_row_offsets, const uint32_t* cache_offsets,
+                          int32_t batch, int32_t buffer_length, int32_t kv_lora_rank,
+                          int32_t rope_dim, const void* w_k_e4m3, const float* w_k_scale,
+                          int32_t n_out, const VOperands& v, void* k_latent_buffer,
+                          void* k_buffer, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, void* stream) {
+    bool empty = false;
+    pkm_status st = check_decompress_sizes(batch, buffer_length, kv_lora_rank, rope_dim, n_out,
+                                           &empty);
+    if (st != PKM_OK || empty) return st;
+    st = check_decompress(cache, layer_idx, buffer_row_offsets, cache_offsets, batch,
+                                     buffer_length, kv_lora_rank, rope_dim, w_k_e4m3, n_out,
+                                     k_latent_buffer, k_buffer);
+    if (st != PKM_OK) return st;
+    if (w_k_scale == nullptr || workspace == nullptr) return PKM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKM_ERR_INVALID_ARG;
+    if (kv_lora_rank % 128 != 0 || kv_lora_rank > 512 || n_out % 128 != 0)
+        return PKM_ERR_UNSUPPORTED;
+    if (workspace_bytes < mla_decompress_k_paged_fp8_workspace_size(buffer_length, kv_lora_rank))
+        return PKM_ERR_INVALID_ARG;
+    const int32_t nv = v.w_uv != nullptr ? v.n_v : 0;
+    DecompressArgs a = make_decompress_args(cache, layer_idx, buffer_row_offsets, cache_offsets,
+                                            batch, buffer_length, kv_lora_rank, rope_dim, n_out,
+                                            k_latent_buffer, k_buffer, dev_status, 128);
+    a.n_tiles_k = a.n_tiles;
+    if (nv > 0) {
+        a.v_buffer = static_cast<uint16_t*>(v.v_buffer);
+        a.n_out_v = nv;
+        a.n_tiles += nv / 128;
+    }
+    a.m_tiles = (buffer_length + 255) / 256;  // CTA-pair tiles of 256 rows
+    a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
+    Fp8Extra x{};
+    x.q_latent = static_cast<uint8_t*>(workspace);
+    x.q_scale = reinterpret_cast<float*>(
+        static_cast<uint8_t*>(workspace) +
+        align256(static_cast<size_t>(buffer_length) * static_cast<size_t>(kv_lora_rank)));
+    x.w_scale = w_k_scale;
+    x.w_scale_v = nv > 0 ? v.w_uv_scale : nullptr;
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
+    alignas(64) CUtensorMap tm_q, tm_w, tm_wv;
+    if (!encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.q_latent, kv_lora_rank, buffer_length,
+                   static_cast<uint64_t>(kv_lora_rank), 128, 128) ||
+        !encode_kblocks_3d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_k_e4m3, 128, n_out,
+                           kv_lora_rank / 128, static_cast<uint64_t>(kv_lora_rank), 128, 64,
+                           kv_lora_rank / 128))
+        return PKM_ERR_CUDA;
+    if (nv > 0) {
+        if (!encode_kblocks_3d(&tm_wv, CU_TENSOR_MAP_DATA_TYPE_UINT8, v.w_uv, 128, nv,
+                               kv_lora_rank / 128, static_cast<uint64_t>(kv_lora_rank), 128, 64,
+                               kv_lora_rank / 128))
+            return PKM_ERR_CUDA;
+    } else {
+        tm_wv = tm_w;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pkm::launch_fp8_gather_quantize(a, x, sms, s) != cudaSuccess) return PKM_ERR_CUDA;
+    return pkm::launch_decompress_fp8_gemm(tm_q, tm_w, tm_wv, a, x, sms, s) == cudaSuccess
+               ? PKM_OK
+               : PKM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkm_status mla_decompress_k_paged(const pkm_paged_cache* cache, uint32_t layer_idx,
+                                  const uint32_t* buffer_row_offsets,
+                                  const uint32_t* cache_offsets, int32_t batch,
+                                  int32_t buffer_length, int32_t kv_lora_rank, int32_t rope_dim,
+                                  const void* w_k, int32_t n_out, void* k_latent_buffer,
+                                  void* k_buffer, int32_t* dev_status, void* stream) {
+    return decompress_bf16(cache, layer_idx, buffer_row_offsets, cache_offsets, batch,
+                           buffer_length, kv_lora_rank, rope_dim, w_k, n_out, VOperands{},
+                           k_latent_buffer, k_buffer, dev_status, stream);
+}
+
+pkm_status mla_decompress_kv_paged(const pkm_paged_cache* cache, uint32_t layer_idx,
+                                   const uint32_t* buffer_row_offsets,
+                                   const uint32_t* cache_offsets, int32_t batch,
+                                   int32_t buffer_length, int32_t kv_lora_rank, int32_t rope_dim,
+                                   const void* w_k, int32_t n_out, const void* w_uv,
+                                   int32_t num_heads, int32_t v_head_dim, void* k_latent_buffer,
+                                   void* k_buffer, void* v_buffer, int32_t* dev_status,
+                                   void* stream) {
+    bool empty = false;
+    pkm_status st = check_decompress_sizes(batch, buffer_length, kv_lora_rank, rope_dim, n_out,
+                                           &empty);
+    if (st != PKM_OK || empty) return st;
+    VOperands v{w_uv, nullptr, 0, v_buffer};
+    st = check_v(v, num_heads, v_head_dim, 64);
+    if (st != PKM_OK) return st;
+    v.n_v = num_heads * v_head_dim;
+    return decompress_bf16(cache, layer_idx, buffer_row_offsets, cache_offsets, batch,
+                           buffer_length, kv_lora_rank, rope_dim, w_k, n_out, v,
+                           k_latent_buffer, k_buffer, dev_status, stream);
 }
 
 size_t mla_decompress_k_paged_fp8_workspace_size(int32_t buffer_length, int32_t kv_lora_rank) {
@@ -267,45 +408,36 @@ pkm_status mla_decompress_k_paged_fp8(const pkm_paged_cache* cache, uint32_t lay
                                       const float* w_k_scale, int32_t n_out,
                                       void* k_latent_buffer, void* k_buffer, void* workspace,
                                       size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    return decompress_fp8(cache, layer_idx, buffer_row_offsets, cache_offsets, batch,
+                          buffer_length, kv_lora_rank, rope_dim, w_k_e4m3, w_k_scale, n_out,
+                          VOperands{}, k_latent_buffer, k_buffer, workspace, workspace_bytes,
+                          dev_status, stream);
+}
+
+pkm_status mla_decompress_kv_paged_fp8(const pkm_paged_cache* cache, uint32_t layer_idx,
+                                       const uint32_t* buffer_row_offsets,
+                                       const uint32_t* cache_offsets, int32_t batch,
+                                       int32_t buffer_length, int32_t kv_lora_rank,
+                                       int32_t rope_dim, const void* w_k_e4m3,
+                                       const float* w_k_scale, int32_t n_out,
+                                       const void* w_uv_e4m3, const float* w_uv_scale,
+                                       int32_t num_heads, int32_t v_head_dim,
+                                       void* k_latent_buffer, void* k_buffer, void* v_buffer,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t* dev_status, void* stream) {
     bool empty = false;
     pkm_status st = check_decompress_sizes(batch, buffer_length, kv_lora_rank, rope_dim, n_out,
                                            &empty);
     if (st != PKM_OK || empty) return st;
-    st = check_decompress(cache, layer_idx, buffer_row_offsets, cache_offsets, batch,
-                                     buffer_length, kv_lora_rank, rope_dim, w_k_e4m3, n_out,
-                                     k_latent_buffer, k_buffer);
+    VOperands v{w_uv_e4m3, w_uv_scale, 0, v_buffer};
+    st = check_v(v, num_heads, v_head_dim, 128);
     if (st != PKM_OK) return st;
-    if (w_k_scale == nullptr || workspace == nullptr) return PKM_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKM_ERR_INVALID_ARG;
-    if (kv_lora_rank % 128 != 0 || kv_lora_rank > 512 || n_out % 128 != 0)
-        return PKM_ERR_UNSUPPORTED;
-    if (workspace_bytes < mla_decompress_k_paged_fp8_workspace_size(buffer_length, kv_lora_rank))
-        return PKM_ERR_INVALID_ARG;
-    DecompressArgs a = make_decompress_args(cache, layer_idx, buffer_row_offsets, cache_offsets,
-                                            batch, buffer_length, kv_lora_rank, rope_dim, n_out,
-                                            k_latent_buffer, k_buffer, dev_status, 128);
-    a.m_tiles = (buffer_length + 255) / 256;  // CTA-pair tiles of 256 rows
-    a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
-    Fp8Extra x{};
-    x.q_latent = static_cast<uint8_t*>(workspace);
-    x.q_scale = reinterpret_cast<float*>(
-        static_cast<uint8_t*>(workspace) +
-        align256(static_cast<size_t>(buffer_length) * static_cast<size_t>(kv_lora_rank)));
-    x.w_scale = w_k_scale;
-    int sms = 0;
-    if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
-    alignas(64) CUtensorMap tm_q, tm_w;
-    if (!encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.q_latent, kv_lora_rank, buffer_length,
-                   static_cast<uint64_t>(kv_lora_rank), 128, 128) ||
-        !encode_kblocks_3d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_k_e4m3, 128, n_out,
-                           kv_lora_rank / 128, static_cast<uint64_t>(kv_lora_rank), 128, 64,
-                           kv_lora_rank / 128))
-        return PKM_ERR_CUDA;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (pkm::launch_fp8_gather_quantize(a, x, sms, s) != cudaSuccess) return PKM_ERR_CUDA;
-    return pkm::launch_decompress_fp8_gemm(tm_q, tm_w, a, x, sms, s) == cudaSuccess
-               ? PKM_OK
-               : PKM_ERR_CUDA;
+    if (w_uv_scale == nullptr) return PKM_ERR_INVALID_ARG;
+    v.n_v = num_heads * v_head_dim;
+    return decompress_fp8(cache, layer_idx, buffer_row_offsets, cache_offsets, batch,
+                          buffer_length, kv_lora_rank, rope_dim, w_k_e4m3, w_k_scale, n_out, v,
+                          k_latent_buffer, k_buffer, workspace, workspace_bytes, dev_status,
+                          stream);
 }
 
 pkm_status kv_matmul_paged(const void* hidden_state, const uint32_t* input_row_offsets,

@@ -4,7 +4,10 @@
 // description and Args: rows [buffer_row_offsets[b], buffer_row_offsets[b+1]) of the
 // ragged buffer receive the latent K rows of cache tokens starting at cache_offsets[b];
 // they are copied to k_latent_buffer and their first kv_lora_rank columns are multiplied
-// by W_k^T into k_buffer.
+// by W_k^T into k_buffer.  With w_uv (mla_prefill_decode_graph_fp8, Args w_uv: "projecting
+// latent values to V", [num_heads, v_head_dim, kv_latent_dim]) the same gathered rows are
+// also multiplied by w_uv^T into v_buffer: the V tiles follow the K tiles of each 256-row
+// block, so the rows are gathered once for both.
 //
 // The grid is made of clusters of two CTAs on two SMs (a CTA pair).  A pair computes
 // 256 x bn output tiles with tcgen05.mma.cta_group::2 (M = 256): each CTA gathers and keeps
@@ -89,6 +92,7 @@ static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decompress_bf16_kernel(const __grid_constant__ CUtensorMap tm_w,
+                           const __grid_constant__ CUtensorMap tm_wv,
                            const __grid_constant__ CUtensorMap tm_cache, const DecompressArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -136,6 +140,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tm_w);
+        if (a.n_tiles > a.n_tiles_k) tma_prefetch_map(&tm_wv);
         if (a.gather_tma) tma_prefetch_map(&tm_cache);
     }
     // The first block's row sources, one row per thread: each is a chain of dependent
@@ -164,7 +169,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t last_phase[kStages] = {};
             bool ok = true;
             for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid() && ok; w.next()) {
-                const int n = w.n;
+                // n tiles [0, n_tiles_k) project with W_k, the rest with w_uv
+                const bool v_tile = w.n >= a.n_tiles_k;
+                const CUtensorMap* wmap = v_tile ? &tm_wv : &tm_w;
+                const int n = v_tile ? w.n - a.n_tiles_k : w.n;
                 for (int kb = 0; kb < KB; ++kb, ++it, rp.next(kStages)) {
                     if ((it & 1u) != who) continue;
                     const uint32_t s = rp.stage, ph = rp.phase;
@@ -174,7 +182,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     if (leader)  // both halves complete on the even CTA's barrier
                         mbar_arrive_expect_tx(&bars->b_full[s], static_cast<uint32_t>(bn) * 128);
-                    tma_load_2d_pair(sB + s * kBStageBytes, &tm_w,
+                    tma_load_2d_pair(sB + s * kBStageBytes, wmap,
                                      mapa_shared(smem_u32(&bars->b_full[s]), 0), kb * 64,
                                      n * bn + static_cast<int>(rank) * half, keep);
                     issued[s] = true;
@@ -337,18 +345,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t tile_i = 0;
         const uint32_t stage = smem_u32(sOut + q * kOutBufBytes);
         int64_t cur_m = -1;
-        uint16_t* row0 = a.k_buffer;  // first row of this warp's 32-row slab
-        uint32_t valid = 0;           // bit r: slab row r is a buffer row with a source
+        uint16_t* row0 = a.k_buffer;   // first row of this warp's 32-row slab, in k_buffer
+        uint16_t* row0v = a.v_buffer;  // and in v_buffer
+        uint32_t valid = 0;            // bit r: slab row r is a buffer row with a source
         for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid(); w.next()) {
             const int64_t m_pair = w.m;
-            const int n = w.n;
             if (m_pair != cur_m) {
                 cur_m = m_pair;
                 const int64_t first = (m_pair * 2 + rank) * kBM + q * 32;
                 row0 = a.k_buffer + first * a.n_out;
+                if (a.v_buffer != nullptr) row0v = a.v_buffer + first * a.n_out_v;
                 valid = __ballot_sync(0xffffffffu,
                                       decompress_row_source(a, first + lane, row_end) >= 0);
             }
+            const bool v_tile = w.n >= a.n_tiles_k;
+            uint16_t* out = v_tile ? row0v + (w.n - a.n_tiles_k) * bn : row0 + w.n * bn;
+            const int64_t pitch = v_tile ? a.n_out_v : a.n_out;
             const uint32_t acc = tile_i & 1, ph = (tile_i >> 1) & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&bars->t_full[acc], ph, wc))) break;
             tc_fence_after();
@@ -366,7 +378,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     p[16 + j] =
                         pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
                 }
-                warp_store_rows_32x64(stage, p, row0 + n * bn + c * 64, a.n_out, valid, lane);
+                warp_store_rows_32x64(stage, p, out + c * 64, pitch, valid, lane);
             }
             tc_fence_before();
             __syncwarp();
@@ -384,8 +396,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_decompress_bf16(const CUtensorMap& tm_w, const CUtensorMap& tm_cache,
-                                   DecompressArgs args, int num_sms, cudaStream_t stream) {
+cudaError_t launch_decompress_bf16(const CUtensorMap& tm_w, const CUtensorMap& tm_wv,
+                                   const CUtensorMap& tm_cache, DecompressArgs args, int num_sms,
+                                   cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(decompress_bf16_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
@@ -393,7 +406,7 @@ cudaError_t launch_decompress_bf16(const CUtensorMap& tm_w, const CUtensorMap& t
     const int64_t max_pairs = num_sms / 2;
     const int64_t pairs = args.total_tiles < max_pairs ? args.total_tiles : max_pairs;
     decompress_bf16_kernel<<<static_cast<unsigned>(2 * pairs), kThreads, kSmemBytes, stream>>>(
-        tm_w, tm_cache, args);
+        tm_w, tm_wv, tm_cache, args);
     return cudaGetLastError();
 }
 

@@ -13,7 +13,8 @@
 //      (s = amax / 448, q = e4m3_rne_satfinite(x / s), fp32) into the workspace.  Every
 //      row is quantised exactly once, however many n tiles later consume it.
 //   2. decompress_fp8_gemm_kernel: clusters of two CTAs (a CTA pair) over 256 x 128 output
-//      tiles (one n tile = one weight-scale block).  Each CTA brings its 128 rows of the
+//      tiles (one n tile = one weight-scale block; with w_uv the V tiles follow the K tiles
+//      and reuse the same quantised rows).  Each CTA brings its 128 rows of the
 //      quantised A tile (resident for the pair's range segment) and its 64-row half of the
 //      tile's 128 x kv_lora_rank e4m3 W_k slice (one 3-D TMA operation, all k-blocks) into a
 //      4-tile ring; the even CTA issues
@@ -142,6 +143,7 @@ __device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t adesc, u
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decompress_fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_q,
                                const __grid_constant__ CUtensorMap tm_w,
+                               const __grid_constant__ CUtensorMap tm_wv,
                                const DecompressArgs a, const Fp8Extra x) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -184,6 +186,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tm_q);
         tma_prefetch_map(&tm_w);
+        if (a.n_tiles > a.n_tiles_k) tma_prefetch_map(&tm_wv);
     }
     tc_fence_before();
     __syncthreads();
@@ -203,7 +206,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid() && ok; w.next()) {
                 const int64_t m_pair = w.m;
-                const int n = w.n;
+                // n tiles [0, n_tiles_k) project with W_k, the rest with w_uv
+                const bool v_tile = w.n >= a.n_tiles_k;
+                const CUtensorMap* wmap = v_tile ? &tm_wv : &tm_w;
+                const int n = v_tile ? w.n - a.n_tiles_k : w.n;
                 if (m_pair != cur_m) {
                     cur_m = m_pair;
                     if (seg > 0 && !mbar_wait(&bars->a_empty, (seg - 1) & 1, wc)) break;
@@ -224,7 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (leader)
                         mbar_arrive_expect_tx(&bars->b_full[s],
                                               2u * static_cast<uint32_t>(KB) * kBKBlockBytes);
-                    tma_load_3d_pair(sB + s * kBStageBytes, &tm_w,
+                    tma_load_3d_pair(sB + s * kBStageBytes, wmap,
                                      mapa_shared(smem_u32(&bars->b_full[s]), 0), 0,
                                      n * kBN + static_cast<int>(rank) * (kBN / 2), 0, keep);
                     rp.next(kStages);
@@ -285,19 +291,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t t_empty_leader = mapa_shared(smem_u32(&bars->t_empty[0]), 0);
         uint32_t tile_i = 0;
         int64_t cur_m = -1;
-        uint16_t* row0 = a.k_buffer;  // first row of this warp's 32-row slab
-        uint32_t valid = 0;           // bit r: slab row r is a buffer row with a source
+        uint16_t* row0 = a.k_buffer;   // first row of this warp's 32-row slab, in k_buffer
+        uint16_t* row0v = a.v_buffer;  // and in v_buffer
+        uint32_t valid = 0;            // bit r: slab row r is a buffer row with a source
         float sa[kKBMax] = {0.f, 0.f, 0.f, 0.f};
         bool ok = true;
         for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid() && ok; w.next()) {
             const int64_t m_pair = w.m;
-            const int n = w.n;
+            const bool v_tile = w.n >= a.n_tiles_k;
+            const int n = v_tile ? w.n - a.n_tiles_k : w.n;
+            const float* wscale = v_tile ? x.w_scale_v : x.w_scale;
             if (m_pair != cur_m) {
                 cur_m = m_pair;
                 const int64_t first = (m_pair * 2 + rank) * kBM + q * 32;
                 const int64_t my_row = first + lane;
                 const bool my_valid = decompress_row_source(a, my_row, row_end) >= 0;
                 row0 = a.k_buffer + first * a.n_out;
+                if (a.v_buffer != nullptr) row0v = a.v_buffer + first * a.n_out_v;
                 valid = __ballot_sync(0xffffffffu, my_valid);
 #pragma unroll
                 for (int kb = 0; kb < kKBMax; ++kb)
@@ -306,7 +316,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float ws[kKBMax];  // this n tile's weight scales, loaded before the first wait
 #pragma unroll
             for (int kb = 0; kb < kKBMax; ++kb)
-                ws[kb] = kb < KB ? __ldg(x.w_scale + static_cast<int64_t>(n) * KB + kb) : 0.0f;
+                ws[kb] = kb < KB ? __ldg(wscale + static_cast<int64_t>(n) * KB + kb) : 0.0f;
             float acc[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
@@ -342,7 +352,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t p[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) p[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
-            warp_store_rows_32x64(stage, p, row0 + n * kBN + h * 64, a.n_out, valid, lane);
+            if (v_tile)
+                warp_store_rows_32x64(stage, p, row0v + n * kBN + h * 64, a.n_out_v, valid, lane);
+            else
+                warp_store_rows_32x64(stage, p, row0 + n * kBN + h * 64, a.n_out, valid, lane);
             ++tile_i;
         }
     }
@@ -368,7 +381,7 @@ cudaError_t launch_fp8_gather_quantize(DecompressArgs args, Fp8Extra extra, int 
 }
 
 cudaError_t launch_decompress_fp8_gemm(const CUtensorMap& tm_q, const CUtensorMap& tm_w,
-                                       DecompressArgs args,
+                                       const CUtensorMap& tm_wv, DecompressArgs args,
                                        Fp8Extra extra, int num_sms, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(decompress_fp8_gemm_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -377,7 +390,7 @@ cudaError_t launch_decompress_fp8_gemm(const CUtensorMap& tm_q, const CUtensorMa
     const int64_t max_pairs = num_sms / 2;
     const int64_t pairs = args.total_tiles < max_pairs ? args.total_tiles : max_pairs;
     decompress_fp8_gemm_kernel<<<static_cast<unsigned>(2 * pairs), kThreads, kSmemBytes, stream>>>(
-        tm_q, tm_w, args, extra);
+        tm_q, tm_w, tm_wv, args, extra);
     return cudaGetLastError();
 }
 

@@ -27,11 +27,14 @@ struct DecompressArgs {
     int32_t n_out;                 // N
     uint16_t* k_latent;            // [L, C] bf16
     uint16_t* k_buffer;            // [L, N] bf16
+    uint16_t* v_buffer;            // [L, N_v] bf16, or null (no V up-projection)
+    int32_t n_out_v;               // N_v = num_heads * v_head_dim (0 without V)
     int32_t* status;               // nullable
     uint64_t timeout_ns;
     // tiling, filled by the launcher
     int32_t bn;                    // N tile
-    int32_t n_tiles;               // N / bn
+    int32_t n_tiles;               // (N + N_v) / bn: K tiles first, then V tiles
+    int32_t n_tiles_k;             // N / bn
     int32_t m_tiles;               // ceil(L / rows per tile)
     int64_t total_tiles;           // m_tiles * n_tiles
     int32_t gather_tma;            // bf16 kernel: the cache gather map is valid (page_size >= 8)
@@ -41,6 +44,7 @@ struct Fp8Extra {
     uint8_t* q_latent;             // [L, R] e4m3 (workspace)
     float* q_scale;                // [L, R/128] (workspace)
     const float* w_scale;          // [N/128, R/128]
+    const float* w_scale_v;        // [N_v/128, R/128], or null
 };
 
 // One kv_matmul problem, already validated.
@@ -65,12 +69,13 @@ struct KvMatmulArgs {
 
 // Launchers (return a CUDA error code; 0 = success).  Tensor maps are encoded by the
 // caller.
-cudaError_t launch_decompress_bf16(const CUtensorMap& tm_w, const CUtensorMap& tm_cache,
-                                   DecompressArgs args, int num_sms, cudaStream_t stream);
+cudaError_t launch_decompress_bf16(const CUtensorMap& tm_w, const CUtensorMap& tm_wv,
+                                   const CUtensorMap& tm_cache, DecompressArgs args, int num_sms,
+                                   cudaStream_t stream);
 cudaError_t launch_fp8_gather_quantize(DecompressArgs args, Fp8Extra extra, int num_sms,
                                        cudaStream_t stream);
 cudaError_t launch_decompress_fp8_gemm(const CUtensorMap& tm_q, const CUtensorMap& tm_w,
-                                       DecompressArgs args,
+                                       const CUtensorMap& tm_wv, DecompressArgs args,
                                        Fp8Extra extra, int num_sms, cudaStream_t stream);
 cudaError_t launch_kv_matmul(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                              KvMatmulArgs args, int num_sms, cudaStream_t stream);

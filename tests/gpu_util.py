@@ -69,6 +69,14 @@ class DeviceDecompress:
                                    device="cuda")
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
         self.fp8 = fp8
+        # the V up-projection rides along when the problem carries a w_uv
+        wv = d.w_uv_e4m3 if fp8 else d.w_uv
+        self.w_uv = dev(wv) if wv is not None else None
+        self.w_uv_scale = dev(d.w_uv_scale) if (fp8 and wv is not None) else None
+        self.v_buffer = None
+        if wv is not None:
+            self.v_buffer = torch.full((L, wv.shape[0], wv.shape[1]), _i16(SENTINEL_OUT),
+                                       dtype=torch.int16, device="cuda")
         if fp8:
             self.w = dev(d.w_k_e4m3)
             self.w_scale = dev(d.w_k_scale)
@@ -80,6 +88,17 @@ class DeviceDecompress:
     def run(self, stream=None, check=True):
         import paged_kv_mla_gb300 as pkm
         d = self.d
+        if self.w_uv is not None and self.fp8:
+            return pkm.mla_decompress_kv_paged_fp8(
+                self.pc, d.layer_idx, self.bro, self.co, d.buffer_length, d.kv_lora_rank,
+                d.rope_dim, self.w, self.w_scale, self.w_uv, self.w_uv_scale, self.k_latent,
+                self.k_buffer, self.v_buffer, self.workspace, dev_status=self.status,
+                stream=stream, check=check)
+        if self.w_uv is not None:
+            return pkm.mla_decompress_kv_paged(
+                self.pc, d.layer_idx, self.bro, self.co, d.buffer_length, d.kv_lora_rank,
+                d.rope_dim, self.w, self.w_uv, self.k_latent, self.k_buffer, self.v_buffer,
+                dev_status=self.status, stream=stream, check=check)
         if self.fp8:
             return pkm.mla_decompress_k_paged_fp8(
                 self.pc, d.layer_idx, self.bro, self.co, d.buffer_length, d.kv_lora_rank,
@@ -95,6 +114,10 @@ class DeviceDecompress:
         L = self.d.buffer_length
         return (host_u16(self.k_latent)[:L], host_u16(self.k_buffer)[:L],
                 int(self.status.item()))
+
+    def v_results(self):
+        torch.cuda.synchronize()
+        return host_u16(self.v_buffer)[:self.d.buffer_length]
 
     def fp8_workspace(self):
         import paged_kv_mla_gb300 as pkm

@@ -32,7 +32,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ["mla_decompress_k_paged", "mla_decompress_k_paged_fp8",
+    for n in ["mla_decompress_k_paged", "mla_decompress_k_paged_fp8", "mla_decompress_kv_paged",
+              "mla_decompress_kv_paged_fp8",
               "mla_decompress_k_paged_fp8_workspace_size", "kv_matmul_paged", "pkm_status_string"]:
         assert n in names
 
@@ -98,6 +99,15 @@ def test_invalid_calls_return_status_without_a_gpu(lib):
     assert r == pkm.PKM_ERR_INVALID_ARG                                # cache_lengths missing
     with pytest.raises(pkm.PkmError):
         pkm.mla_decompress_k_paged(good, 0, bro, co, 4, 60, 20, w, t16, t16, stream=0)
+    # K and V: the V operands are checked before anything launches
+    wv = torch.zeros(3 * 20 * 64, dtype=torch.int16).view(3, 20, 64)  # 3 x 20 = 60 columns
+
+    def call_kv(w_uv, L=4, v=t16):
+        return pkm.mla_decompress_kv_paged(good, 0, bro, co, L, 64, 16, w, w_uv, t16, t16, v,
+                                           stream=0, check=False)
+    assert call_kv(wv) == pkm.PKM_ERR_UNSUPPORTED                      # H * Dv not a multiple of 64
+    assert call_kv(torch.zeros(1, 64, 64, dtype=torch.int16), v=t16[1:]) == pkm.PKM_ERR_INVALID_ARG  # misaligned v
+    assert call_kv(wv, L=0) == pkm.PKM_OK                              # nothing to do
 
 
 def test_oracle_and_product_share_no_code():
