@@ -168,6 +168,23 @@ def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
     return units_per_rank * world / seconds
 
 
+def bf16_algorithmic_bytes(d) -> int:
+    """Per covered row: the latent row read (2C bytes) and copied (2C), one bf16 output row
+    per up-projection (2 N, + 2 N_v with V); the weights once."""
+    rows = min(int(d.buffer_row_offsets[-1]), d.buffer_length)
+    n = d.n_out + d.n_out_v
+    return rows * (4 * d.latent_cols + 2 * n) + n * d.kv_lora_rank * 2
+
+
+def fp8_algorithmic_bytes(d) -> int:
+    """As bf16_algorithmic_bytes, plus the quantised row the entry point writes to its
+    workspace (R e4m3 codes and R/128 fp32 scales); e4m3 weights."""
+    rows = min(int(d.buffer_row_offsets[-1]), d.buffer_length)
+    n = d.n_out + d.n_out_v
+    R = d.kv_lora_rank
+    return rows * (4 * d.latent_cols + 2 * n + R + 4 * (R // 128)) + n * R
+
+
 def _device_problem(d, fp8=False):
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from gpu_util import DeviceDecompress
@@ -257,7 +274,7 @@ def run_ours(args, rank, world, local_rank):
     g8 = _device_problem(d8, fp8=True)
     t8 = _time_steps(g8.run, sec_steps, 3, flush, stream) / sec_steps
     assert int(g8.status.item()) == 0
-    b8 = 2 * (d8.buffer_length * (2 * d8.latent_cols + 2 * d8.n_out)) + d8.n_out * d8.kv_lora_rank
+    b8 = fp8_algorithmic_bytes(d8)
     extra["fp8_decompress"] = {
         "workload": d8.name, "rows": d8.buffer_length, "ms": t8 * 1e3,
         "tflops": d8.flops / t8 / 1e12, "rows_per_s": d8.buffer_length / t8,
@@ -273,6 +290,24 @@ def run_ours(args, rank, world, local_rank):
         "tflops": dl.flops / tl / 1e12, "rows_per_s": dl.buffer_length / tl,
         "frac_of_measured_bf16": dl.flops / tl / 1e12 / peaks["bf16_tflops"]}
     del gl
+    # K and V from one gather (w_uv up-projection rides along; same rows and weights shape)
+    for key, wl, fp8 in [("kv_decompress_bf16", "deepseek_v3_bf16_decompress_kv", False),
+                         ("kv_decompress_fp8", "deepseek_v3_fp8_decompress_kv", True)]:
+        dv = workloads.WORKLOADS[wl]()
+        gv = _device_problem(dv, fp8=fp8)
+        tv = _time_steps(gv.run, sec_steps, 3, flush, stream) / sec_steps
+        assert int(gv.status.item()) == 0
+        lv = dv.buffer_length
+        bv = fp8_algorithmic_bytes(dv) if fp8 else bf16_algorithmic_bytes(dv)
+        extra[key] = {
+            "workload": dv.name, "rows": lv, "n_out_k": dv.n_out, "n_out_v": dv.n_out_v,
+            "ms": tv * 1e3, "tflops": dv.flops / tv / 1e12, "rows_per_s": lv / tv,
+            "hbm_gbs": bv / tv / 1e9,
+            "frac": (bv / tv / 1e9 / peaks["hbm_gbs"]) if fp8 else
+                    (dv.flops / tv / 1e12 / peaks["bf16_tflops"]),
+            "frac_of": "measured HBM" if fp8 else "measured bf16 tensor peak",
+            "launches_per_step": 2 if fp8 else 1}
+        del gv, dv
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from gpu_util import DeviceKvMatmul
     km = workloads.WORKLOADS["kv_matmul_write_path"]()
@@ -292,7 +327,7 @@ def run_ours(args, rank, world, local_rank):
     # ---------------- CPU oracle on a bounded sample ----------------
     cpu = cpu_baseline_sample(d, args.cpu_rows)
 
-    algo_bytes = rows * (2 * d.latent_cols * 2 + 2 * d.n_out) + d.n_out * d.kv_lora_rank * 2
+    algo_bytes = bf16_algorithmic_bytes(d)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,

@@ -126,8 +126,14 @@ class DecompressInputs:
 
     @property
     def flops(self) -> int:
+        """K up-projection, plus the V one when the problem carries a w_uv."""
         rows = min(int(self.buffer_row_offsets[-1]), self.buffer_length)
-        return 2 * rows * self.kv_lora_rank * self.n_out
+        return 2 * rows * self.kv_lora_rank * (self.n_out + self.n_out_v)
+
+    @property
+    def n_out_v(self) -> int:
+        wv = self.w_uv if self.w_uv is not None else self.w_uv_e4m3
+        return 0 if wv is None else int(wv.shape[0] * wv.shape[1])
 
 
 def _assign_pages(pages_needed, total_pages, g):
