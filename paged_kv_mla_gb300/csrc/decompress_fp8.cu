@@ -20,10 +20,11 @@
 //      4-tile ring; the even CTA issues
 //      tcgen05.mma.cta_group::2 kind::f8f6f4 (M = 256), accumulating each 128-wide k-block
 //      into its own TMEM accumulator (4 x 128 columns per CTA).  8 epilogue warps per CTA
-//      combine them in registers as sum_kb (s_a[row, kb] * s_w[n_tile, kb]) * acc_kb before
-//      rounding to bf16 and storing k_buffer in whole 128-byte row segments (through a
-//      swizzled 4 KB shared buffer per warp).  An accumulator is released as soon as
-//      the epilogue has read it, so the next tile's MMAs overlap the rest of the epilogue.
+//      read each k-block as soon as its MMAs retire and combine them in registers as
+//      sum_kb (s_a[row, kb] * s_w[n_tile, kb]) * acc_kb before rounding to bf16 and storing
+//      k_buffer in whole 128-byte row segments (through a swizzled 4 KB shared buffer per
+//      warp).  The accumulators go back to the MMAs once per tile, right after the last
+//      k-block is read, so the rounding and stores overlap the next tile's MMAs.
 #include "pkm_device.cuh"
 #include "pkm_internal.h"
 
@@ -116,7 +117,8 @@ struct Bars {
     uint64_t a_full;            // even CTA: both CTAs' A tiles landed
     uint64_t a_empty;           // both CTAs: the MMAs are done with A
     uint64_t t_full[kKBMax];    // both CTAs: k-block accumulator ready
-    uint64_t t_empty[kKBMax];   // even CTA: both CTAs' epilogues read a k-block accumulator
+    uint64_t t_drained;         // even CTA: both CTAs' epilogues read all of a tile's
+                                // accumulators
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -171,10 +173,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bars->a_full, 1);
         mbar_init(&bars->a_empty, 1);
-        for (int i = 0; i < kKBMax; ++i) {
-            mbar_init(&bars->t_full[i], 1);
-            mbar_init(&bars->t_empty[i], 2 * kEpiWarps);
-        }
+        for (int i = 0; i < kKBMax; ++i) mbar_init(&bars->t_full[i], 1);
+        mbar_init(&bars->t_drained, 2 * kEpiWarps);
         mbar_init(&bars->mma_done, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -256,14 +256,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (!mbar_wait(&bars->a_full, seg & 1, wc)) break;
                 }
                 const uint32_t s = rp.stage, ph = rp.phase;
-                if (!mbar_wait(&bars->b_full[s], ph, wc)) break;
+                // the accumulators are handed back once per tile: a wait, a fence and a
+                // commit between the MMAs of every k-block left the tensor pipe idle for a
+                // third of the time
+                if (!mbar_wait(&bars->b_full[s], ph, wc) ||
+                    !mbar_wait(&bars->t_drained, (tile_i & 1) ^ 1, wc))
+                    break;
+                tc_fence_after();
                 const uint32_t b_stage = smem_u32(sB + s * kBStageBytes);
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&bars->t_empty[kb], (tile_i & 1) ^ 1, wc)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
                     const uint32_t a_addr = smem_u32(sA + kb * kABlockBytes);
                     const uint32_t b_addr = b_stage + kb * kBKBlockBytes;
                     const uint32_t d = tmem + static_cast<uint32_t>(kb) * kBN;
@@ -288,7 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
         const uint32_t stage = smem_u32(sOut + (warp - 2) * kOutBufBytes);
-        const uint32_t t_empty_leader = mapa_shared(smem_u32(&bars->t_empty[0]), 0);
+        const uint32_t t_drained_leader = mapa_shared(smem_u32(&bars->t_drained), 0);
         uint32_t tile_i = 0;
         int64_t cur_m = -1;
         uint16_t* row0 = a.k_buffer;   // first row of this warp's 32-row slab, in k_buffer
@@ -336,9 +337,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_ld_x32(tbase, v0);
                 tmem_ld_x32(tbase + 32, v1);
                 tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(t_empty_leader + kb * sizeof(uint64_t));
+                if (kb == KB - 1) {  // every accumulator of the tile has been read
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(t_drained_leader);
+                }
                 // packed FMAs: the two epilogue warps on the MMA warp's scheduler slow its
                 // MMA issue in proportion to the instructions they issue
 #pragma unroll
