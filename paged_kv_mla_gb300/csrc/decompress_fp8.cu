@@ -296,12 +296,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint16_t* row0v = a.v_buffer;  // and in v_buffer
         uint32_t valid = 0;            // bit r: slab row r is a buffer row with a source
         float sa[kKBMax] = {0.f, 0.f, 0.f, 0.f};
+        // weight scales of an n tile (tile id n_any in [0, n_tiles)); the next tile's are
+        // fetched before this tile's rounding and stores, off the first k-block's path
+        auto load_ws = [&](int n_any, float (&dst)[kKBMax]) {
+            const bool vt = n_any >= a.n_tiles_k;
+            const float* src = (vt ? x.w_scale_v : x.w_scale) +
+                               static_cast<int64_t>(vt ? n_any - a.n_tiles_k : n_any) * KB;
+#pragma unroll
+            for (int kb = 0; kb < kKBMax; ++kb) dst[kb] = kb < KB ? __ldg(src + kb) : 0.0f;
+        };
+        float ws[kKBMax];
+        if (t_begin < t_end) load_ws(static_cast<int>(t_begin % a.n_tiles), ws);
         bool ok = true;
         for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid() && ok; w.next()) {
             const int64_t m_pair = w.m;
             const bool v_tile = w.n >= a.n_tiles_k;
             const int n = v_tile ? w.n - a.n_tiles_k : w.n;
-            const float* wscale = v_tile ? x.w_scale_v : x.w_scale;
             if (m_pair != cur_m) {
                 cur_m = m_pair;
                 const int64_t first = (m_pair * 2 + rank) * kBM + q * 32;
@@ -314,10 +324,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < kKBMax; ++kb)
                     sa[kb] = (my_valid && kb < KB) ? x.q_scale[my_row * KB + kb] : 0.0f;
             }
-            float ws[kKBMax];  // this n tile's weight scales, loaded before the first wait
-#pragma unroll
-            for (int kb = 0; kb < kKBMax; ++kb)
-                ws[kb] = kb < KB ? __ldg(wscale + static_cast<int64_t>(n) * KB + kb) : 0.0f;
             float acc[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
@@ -352,6 +358,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
+            if (w.t + 1 < t_end) load_ws(w.n + 1 == a.n_tiles ? 0 : w.n + 1, ws);
             uint32_t p[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) p[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
