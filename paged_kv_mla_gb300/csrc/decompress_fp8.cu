@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(256)
 // 2. block-scaled GEMM
 // ------------------------------------------------------------------------------------
 
-constexpr int kThreads = 320;                 // producer, MMA, 8 epilogue warps
+constexpr int kThreads = 448;                 // producer, MMA, 8 epilogue, 4 store warps
 constexpr int kBM = 128;                      // rows per CTA (256 per pair)
 constexpr int kBN = 128;                      // pair N tile = one weight-scale block
 constexpr int kKBMax = 4;                     // kv_lora_rank <= 512
@@ -108,6 +108,8 @@ constexpr int kStages = 4;
 constexpr int kBKBlockBytes = (kBN / 2) * 128;        // this CTA's 64 weight rows x 128 e4m3
 constexpr int kBStageBytes = kKBMax * kBKBlockBytes;  // a tile's weight half: 32 KB
 constexpr int kEpiWarps = 8;
+constexpr int kStoreWarps = 4;
+constexpr int kFirstStoreWarp = 2 + kEpiWarps;
 constexpr int kOutBufBytes = 32 * 128;
 constexpr uint32_t kTmemCols = 512;           // kKBMax accumulators x 128 columns
 
@@ -119,6 +121,13 @@ struct Bars {
     uint64_t t_full[kKBMax];    // both CTAs: k-block accumulator ready
     uint64_t t_drained;         // even CTA: both CTAs' epilogues read all of a tile's
                                 // accumulators
+    uint64_t st_full;           // the epilogue warps staged a tile's rounded results
+    uint64_t st_empty;          // the store warps wrote them out; the staging is free
+    struct {
+        uint16_t* dst;          // first element of the box in k_buffer / v_buffer
+        int64_t pitch;          // row pitch in elements
+        uint32_t valid;         // bit r: row r of the box is written
+    } box[kEpiWarps];           // where each epilogue warp's staged 32 x 64 box goes
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -175,6 +184,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(&bars->a_empty, 1);
         for (int i = 0; i < kKBMax; ++i) mbar_init(&bars->t_full[i], 1);
         mbar_init(&bars->t_drained, 2 * kEpiWarps);
+        mbar_init(&bars->st_full, kEpiWarps);
+        mbar_init(&bars->st_empty, kStoreWarps);
         mbar_init(&bars->mma_done, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -282,10 +293,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mma_commit_pair(&bars->mma_done, 1);
             mbar_wait(&bars->mma_done, 0, wc, false);
         }
-    } else {
+    } else if (warp < kFirstStoreWarp) {
         // 8 epilogue warps: warp w reads TMEM lane quarter w % 4 (32 rows) and one 64-column
-        // half of the 128-column tile, so each keeps 64 fp32 partial sums and issues both
-        // 32-column TMEM loads of a k-block before waiting once.
+        // half of the 128-column tile and keeps 64 fp32 partial sums.  The rounded results
+        // go to shared memory; the store warps write them out while these warps go on to the
+        // next tile (one SM moves only ~26 bytes per cycle to global memory, so storing a
+        // tile takes about as long as computing it).
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
         const uint32_t stage = smem_u32(sOut + (warp - 2) * kOutBufBytes);
@@ -339,33 +352,74 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const float cs = sa[kb] * ws[kb];
                 const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(kb) * kBN + h * 64;
-                uint32_t v0[32], v1[32];
-                tmem_ld_x32(tbase, v0);
-                tmem_ld_x32(tbase + 32, v1);
-                tmem_ld_wait();
-                if (kb == KB - 1) {  // every accumulator of the tile has been read
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_remote(t_drained_leader);
-                }
-                // packed FMAs: the two epilogue warps on the MMA warp's scheduler slow its
-                // MMA issue in proportion to the instructions they issue
+                // two 32-column halves: 14 warps leave 128 registers a thread
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    fma2(acc[j], acc[j + 1], cs, __uint_as_float(v0[j]), __uint_as_float(v0[j + 1]));
-                    fma2(acc[32 + j], acc[33 + j], cs, __uint_as_float(v1[j]),
-                         __uint_as_float(v1[j + 1]));
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[32];
+                    tmem_ld_x32(tbase + half * 32, v);
+                    tmem_ld_wait();
+                    if (half == 1 && kb == KB - 1) {  // every accumulator has been read
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_remote(t_drained_leader);
+                    }
+                    // packed FMAs: the two epilogue warps on the MMA warp's scheduler slow
+                    // its MMA issue in proportion to the instructions they issue
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2)
+                        fma2(acc[half * 32 + j], acc[half * 32 + j + 1], cs,
+                             __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
                 }
             }
             if (!ok) break;
             if (w.t + 1 < t_end) load_ws(w.n + 1 == a.n_tiles ? 0 : w.n + 1, ws);
-            uint32_t p[32];
+            // stage the rounded box once the store warps have written out the previous one
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->st_empty, (tile_i & 1) ^ 1, wc))) {
+                ok = false;
+                break;
+            }
+            const uint32_t rowaddr = stage + lane * 128;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) p[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
-            if (v_tile)
-                warp_store_rows_32x64(stage, p, row0v + n * kBN + h * 64, a.n_out_v, valid, lane);
-            else
-                warp_store_rows_32x64(stage, p, row0 + n * kBN + h * 64, a.n_out, valid, lane);
+            for (int j = 0; j < 8; ++j)
+                st_shared_v4(rowaddr + ((j ^ (lane & 7)) << 4),
+                             pack_bf16x2(acc[8 * j], acc[8 * j + 1]),
+                             pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
+                             pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]),
+                             pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
+            if (lane == 0) {
+                auto& b = bars->box[warp - 2];
+                b.dst = (v_tile ? row0v : row0) + n * kBN + h * 64;
+                b.pitch = v_tile ? a.n_out_v : a.n_out;
+                b.valid = valid;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->st_full);
+            ++tile_i;
+        }
+    } else {
+        // 4 store warps: store warp s writes out the boxes of epilogue warps 2s and 2s + 1,
+        // each as whole 128-byte row segments (eight lanes per row).
+        const int s = warp - kFirstStoreWarp;
+        const int chunk = lane & 7;
+        uint32_t tile_i = 0;
+        for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid(); w.next()) {
+            if (!mbar_wait(&bars->st_full, tile_i & 1, wc)) break;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int src = 2 * s + e;
+                const uint32_t box = smem_u32(sOut + src * kOutBufBytes);
+                uint16_t* dst = bars->box[src].dst;
+                const int64_t pitch = bars->box[src].pitch;
+                const uint32_t valid = bars->box[src].valid;
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int r = it * 4 + (lane >> 3);
+                    const uint4 v = ld_shared_v4(box + r * 128 + ((chunk ^ (r & 7)) << 4));
+                    if ((valid >> r) & 1u) st_v4(dst + r * pitch + chunk * 8, v);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->st_empty);
             ++tile_i;
         }
     }
