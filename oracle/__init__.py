@@ -9,6 +9,8 @@ Each wrapper follows the passage cited in the C source:
   * generic_flare_mla_decompress_k_cache_ragged_paged -- description and Args
   * mla_prefill_decode_graph_fp8 -- Parameters (scale granularities), Args (w_k, w_k_scale,
     w_uv, w_uv_scale)
+  * mla_prefill_decode_graph_fp8 -- Args kv_input_fn, kv_norm_gamma, epsilon, freqs_cis
+    (the cache-write side)
   * kv_matmul_ragged_paged -- Args (hidden_state, input_row_offsets, weight, kv_collection)
 """
 from __future__ import annotations
@@ -93,6 +95,10 @@ def lib():
                                                                     _u8p, _f32p, _i32, _i32, _i64,
                                                                     _u16p, _u16p, _u16p, _u8p, _f32p]
             L.oracle_decompress_kv_fp8_row.restype = ctypes.c_int
+            L.oracle_cache_write.argtypes = [_u16p, _u32p, _i32, _i32, _i32, _i32, _f32p, ctypes.c_float,
+                                             _f32p, _i32, _u16p, _i64, _i64, _i64, _i32, _i32, _u32p,
+                                             _i32, _u32p, _u32]
+            L.oracle_cache_write.restype = ctypes.c_int
             L.oracle_kv_matmul.argtypes = [_u16p, _u32p, _i32, _i32, _i32, _u16p, _i32, _u16p, _i64,
                                            _i64, _i64, _i64, _i32, _i32, _i32, _u32p, _i32, _u32p,
                                            _u32]
@@ -357,6 +363,20 @@ def decompress_kv_fp8_row(cache: PagedCacheView, layer_idx, bro, co, batch, buff
                                             _c(w_uv_scale, np.float32).reshape(-1), H, Dv, int(r),
                                             lat, k, v, q, s)
     return st, lat, k, v.reshape(H, Dv), q, s
+
+
+def cache_write(latent, input_row_offsets, batch, total_rows, kv_lora_rank, rope_dim, gamma,
+                epsilon, freqs_cis, cache: PagedCacheView, cache_lengths, layer_idx):
+    """RMSNorm + RoPE of new latent rows into the paged cache; cache.data is modified in
+    place.  Returns the status."""
+    freqs_cis = _c(freqs_cis, np.float32)
+    return lib().oracle_cache_write(_c(latent, np.uint16).reshape(-1), _c(input_row_offsets, np.uint32),
+                                    int(batch), int(total_rows), int(kv_lora_rank), int(rope_dim),
+                                    _c(gamma, np.float32), float(epsilon), freqs_cis.reshape(-1),
+                                    int(freqs_cis.shape[0]), cache.data, cache.layer_stride,
+                                    cache.page_stride, cache.slot_stride, cache.num_pages,
+                                    cache.page_size, cache.page_table, cache.max_pages_per_seq,
+                                    _c(cache_lengths, np.uint32), int(layer_idx))
 
 
 def kv_matmul(hidden_state, input_row_offsets, batch, total_rows, weight, cache: PagedCacheView,

@@ -18,6 +18,8 @@
  *     128-column block (the reading of the silent points is stated at each function).
  *   - mla_prefill_decode_graph_fp8, Args w_uv / w_uv_scale: the V up-projection of the same
  *     gathered latent rows (bf16 and block-scaled FP8).
+ *   - mla_prefill_decode_graph_fp8, Args kv_input_fn, kv_norm_gamma, epsilon, freqs_cis: the
+ *     cache-write side (RMSNorm and RoPE of new latent rows, stored into the paged cache).
  *   - kv_matmul_ragged_paged (Modular MAX kernels, nn/kv_cache_ragged), Args: a GEMM on
  *     the ragged hidden_state whose rows are written into the paged cache of one layer,
  *     after each request's existing cache length.
@@ -546,6 +548,79 @@ int oracle_decompress_kv_fp8_row(const uint16_t* cache, int64_t layer_stride,
     fp8_row_product_v(q_row, scale_row, w_uv_e4m3, w_uv_scale, num_heads, v_head_dim,
                       kv_lora_rank, v_row);
     return 0;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Cache-write side of mla_prefill_decode_graph_fp8 (kv_norm_gamma, epsilon, freqs_cis)  */
+/* ------------------------------------------------------------------------------------ */
+
+/*
+ * The graph's Args: kv_input_fn loads "the KV latent values", shape [tot_seq_len,
+ * cache_head_dim]; kv_norm_gamma holds "RMSNorm gamma weights for normalizing the KV
+ * cache", [kv_lora_rank]; epsilon is the RMSNorm constant; freqs_cis holds "precomputed
+ * RoPE frequency values", [max_seq_len, qk_rope_head_dim]; input_row_offsets delimits
+ * each request's rows; kv_collection / layer_idx name the cache.
+ *
+ * Readings of the silent points:
+ *   - row r = iro[b] + i of the new latent values is token position pos = cache_lengths[b]
+ *     + i of request b (the position rule kv_matmul_ragged_paged uses for new tokens) and
+ *     goes to that position's cache slot: logical page pos / page_size through the page
+ *     table, slot pos % page_size;
+ *   - the first R = kv_lora_rank columns are RMS-normalised:
+ *         y_k = x_k * gamma_k / sqrt( (sum_{k<R} x_k^2) / R + epsilon ),
+ *   - the last P = qk_rope_head_dim columns are rotated by freqs_cis[pos], read as P/2
+ *     complex numbers (cos, sin) applied to the interleaved pairs (x_2j, x_2j+1):
+ *         (x_2j, x_2j+1) -> (x_2j * cos - x_2j+1 * sin, x_2j * sin + x_2j+1 * cos),
+ *   - gamma and freqs_cis are fp32; the arithmetic is fp64 here and every result is
+ *     rounded once to bf16.
+ * Nothing else in the cache is written.  Returns 0, or 4 if a row's position resolves
+ * outside the page table / the cache or past max_seq_len (that row is skipped).
+ */
+int oracle_cache_write(const uint16_t* latent, const uint32_t* input_row_offsets,
+                       int32_t batch, int32_t total_rows, int32_t kv_lora_rank,
+                       int32_t rope_dim, const float* gamma, float epsilon,
+                       const float* freqs_cis, int32_t max_seq_len, uint16_t* cache,
+                       int64_t layer_stride, int64_t page_stride, int64_t slot_stride,
+                       int32_t num_pages, int32_t page_size, const uint32_t* page_table,
+                       int32_t max_pages_per_seq, const uint32_t* cache_lengths,
+                       uint32_t layer_idx) {
+    int status = 0;
+    const int32_t C = kv_lora_rank + rope_dim;
+    uint16_t* layer = cache + (int64_t)layer_idx * layer_stride;
+    for (int32_t b = 0; b < batch; ++b) {
+        uint32_t begin = input_row_offsets[b];
+        uint32_t end = input_row_offsets[b + 1];
+        for (uint32_t i = 0; begin + i < end; ++i) {
+            uint64_t r = (uint64_t)begin + i;
+            if (r >= (uint64_t)total_rows) break;
+            uint64_t pos = (uint64_t)cache_lengths[b] + i;
+            int64_t off = token_offset(page_table, max_pages_per_seq, num_pages, page_size,
+                                       page_stride, slot_stride, b, pos);
+            if (off < 0 || pos >= (uint64_t)max_seq_len) {
+                status = 4;
+                continue;
+            }
+            const uint16_t* x = latent + r * (uint64_t)C;
+            uint16_t* y = layer + off;
+            double sumsq = 0.0;
+            for (int32_t k = 0; k < kv_lora_rank; ++k) {
+                double v = oracle_bf16_to_double(x[k]);
+                sumsq += v * v;
+            }
+            double inv = 1.0 / sqrt(sumsq / (double)kv_lora_rank + (double)epsilon);
+            for (int32_t k = 0; k < kv_lora_rank; ++k)
+                y[k] = oracle_double_to_bf16(oracle_bf16_to_double(x[k]) * inv * (double)gamma[k]);
+            const float* f = freqs_cis + pos * (uint64_t)rope_dim;
+            for (int32_t j = 0; j < rope_dim / 2; ++j) {
+                double x0 = oracle_bf16_to_double(x[kv_lora_rank + 2 * j]);
+                double x1 = oracle_bf16_to_double(x[kv_lora_rank + 2 * j + 1]);
+                double c = (double)f[2 * j], sn = (double)f[2 * j + 1];
+                y[kv_lora_rank + 2 * j] = oracle_double_to_bf16(x0 * c - x1 * sn);
+                y[kv_lora_rank + 2 * j + 1] = oracle_double_to_bf16(x0 * sn + x1 * c);
+            }
+        }
+    }
+    return status;
 }
 
 /* ------------------------------------------------------------------------------------ */

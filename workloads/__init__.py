@@ -35,6 +35,7 @@ PAGE_TABLE_PAD = 0xFFFFFFFF  # unused page-table entries (never read by a correc
 SENTINEL_K = 0x7FA1          # bf16 NaN patterns no finite product can produce
 SENTINEL_V = 0x7FA2
 SENTINEL_OUT = 0x7FA3
+SENTINEL_CACHE = 0x7FA4      # latent-cache slots a cache write must leave alone
 
 
 def _gen(seed: int) -> torch.Generator:
@@ -250,6 +251,99 @@ def long_context_decompress(seed=1003) -> DecompressInputs:
 
 
 @dataclass
+class CacheWriteInputs:
+    """New latent rows [total_rows, R + P] to be normalised, rotated and stored into a paged
+    latent cache [num_layers, num_pages, page_size, R + P] after each request's cached
+    tokens."""
+    name: str
+    latent: np.ndarray             # uint16 bf16 [total_rows, R + P]
+    input_row_offsets: np.ndarray  # uint32 [batch + 1]
+    cache_lengths: np.ndarray      # uint32 [batch]
+    page_table: np.ndarray         # uint32 [batch, max_pages_per_seq]
+    cache: np.ndarray              # uint16 bf16, pre-filled with SENTINEL_CACHE
+    gamma: np.ndarray              # float32 [R]
+    epsilon: float
+    freqs_cis: np.ndarray          # float32 [max_seq_len, P]: P/2 (cos, sin) pairs per position
+    kv_lora_rank: int
+    rope_dim: int
+    layer_idx: int
+
+    @property
+    def batch(self) -> int:
+        return int(self.page_table.shape[0])
+
+    @property
+    def total_rows(self) -> int:
+        return int(self.latent.shape[0])
+
+    @property
+    def row_elems(self) -> int:
+        return self.kv_lora_rank + self.rope_dim
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.cache.shape[1])
+
+    @property
+    def page_size(self) -> int:
+        return int(self.cache.shape[2])
+
+    @property
+    def strides(self):
+        L, Pg, S, E = self.cache.shape
+        return Pg * S * E, S * E, E
+
+    @property
+    def bytes_moved(self) -> int:
+        """Algorithmic HBM bytes: read every new row, write it into the cache (bf16)."""
+        rows = int(self.input_row_offsets[-1])
+        return 2 * rows * self.row_elems * 2
+
+
+def make_cache_write(name, seed, new_tokens, cache_lengths, kv_lora_rank, rope_dim, page_size,
+                     num_layers=1, layer_idx=0, extra_pages=0, epsilon=1e-6, max_seq_len=None,
+                     latent_std=1.0) -> CacheWriteInputs:
+    """Seeded cache-write problem: latent ~N(0, latent_std^2) bf16, gamma ~1 + N(0, 0.1^2)
+    fp32, freqs_cis = (cos phi, sin phi) for phi ~U[0, 2 pi) drawn per position and pair
+    (any unit complex numbers are valid RoPE factors), pages assigned in one seeded
+    shuffle, the cache filled with SENTINEL_CACHE."""
+    g = _gen(seed)
+    new_tokens = np.asarray(new_tokens, np.int64)
+    cl = np.asarray(cache_lengths, np.int64)
+    B = len(new_tokens)
+    iro = np.zeros(B + 1, np.uint32)
+    iro[1:] = np.cumsum(new_tokens)
+    C = kv_lora_rank + rope_dim
+    pages_needed = [int(math.ceil((cl[b] + new_tokens[b]) / page_size)) for b in range(B)]
+    total_pages = sum(pages_needed) + extra_pages
+    pt = _assign_pages(pages_needed, total_pages, g)
+    M = int(iro[-1])
+    latent = bf16_normal((M, C), latent_std, g)
+    gamma = (1.0 + 0.1 * torch.randn(kv_lora_rank, generator=g, dtype=torch.float64)).to(torch.float32)
+    if max_seq_len is None:
+        max_seq_len = int((cl + new_tokens).max()) + 1
+    phi = torch.rand(max_seq_len, rope_dim // 2, generator=g, dtype=torch.float64) * (2 * math.pi)
+    freqs = torch.stack([torch.cos(phi), torch.sin(phi)], dim=-1).reshape(max_seq_len, rope_dim)
+    cache = np.full((num_layers, total_pages, page_size, C), SENTINEL_CACHE, np.uint16)
+    return CacheWriteInputs(name=name, latent=latent, input_row_offsets=iro,
+                            cache_lengths=cl.astype(np.uint32), page_table=pt, cache=cache,
+                            gamma=gamma.numpy().copy(), epsilon=float(epsilon),
+                            freqs_cis=freqs.to(torch.float32).numpy().copy(),
+                            kv_lora_rank=kv_lora_rank, rope_dim=rope_dim, layer_idx=layer_idx)
+
+
+def cache_write_path(seed=1007) -> CacheWriteInputs:
+    """DeepSeek-V3 latent cache write of a prefill batch: 32 requests, new ~U[1024, 4096]
+    tokens after cache_len ~U[0, 2048], latent 512 + 64, page_size 128, 2 layers (layer 1
+    written)."""
+    g = _gen(seed)
+    new = torch.randint(1024, 4097, (32,), generator=g).numpy()
+    cl = torch.randint(0, 2049, (32,), generator=g).numpy()
+    return make_cache_write("cache_write_path", seed + 1, new, cl, 512, 64, 128, num_layers=2,
+                            layer_idx=1)
+
+
+@dataclass
 class KvMatmulInputs:
     """One kv_matmul problem.  cache is [num_layers, 2 (K, V), num_pages, page_size,
     head_elems]; hidden_state [total_rows, k_in]; weight [k_in, n_out] (n_out contiguous)."""
@@ -353,4 +447,5 @@ WORKLOADS = {
     "deepseek_v3_bf16_decompress_kv": lambda: deepseek_decompress_kv(1001, fp8=False),
     "deepseek_v3_fp8_decompress_kv": lambda: deepseek_decompress_kv(1001, fp8=True),
     "kv_matmul_write_path": kv_matmul_write_path,
+    "cache_write_path": cache_write_path,
 }
