@@ -50,6 +50,7 @@ KERNEL_SOURCES = {
     "decompress_fp8_gemm_kernel": ["decompress_fp8.cu"],
     "fp8_gather_quantize_kernel": ["decompress_fp8.cu"],
     "kv_matmul_kernel": ["kv_matmul.cu"],
+    "cache_write_kernel": ["cache_write.cu"],
 }
 
 
@@ -220,9 +221,13 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     peaks, peak_kind = load_peaks()
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
     def flush():
+        # write a buffer larger than L2, then read another one: the timed step starts with
+        # no line of its inputs in L2 and no dirty line of the flush left to write back
         flush_buf.fill_(1)
+        flush_read.max()
 
     dist = None
     if world > 1:
@@ -320,6 +325,17 @@ def run_ours(args, rank, world, local_rank):
         "tflops": km.flops / tk / 1e12, "gbs": km.bytes_moved / tk / 1e9,
         "roofline_frac": t_roof / tk}
     del gk
+    from gpu_util import DeviceCacheWrite
+    cw = workloads.WORKLOADS["cache_write_path"]()
+    gc = DeviceCacheWrite(cw)
+    tc = _time_steps(gc.run, sec_steps, 3, flush, stream) / sec_steps
+    assert int(gc.status.item()) == 0
+    extra["cache_write"] = {
+        "workload": cw.name, "rows": cw.total_rows, "ms": tc * 1e3,
+        "rows_per_s": cw.total_rows / tc, "gbs": cw.bytes_moved / tc / 1e9,
+        "hbm_frac_of_measured": cw.bytes_moved / tc / 1e9 / peaks["hbm_gbs"],
+        "traffic": profiled_traffic("cache_write_kernel"), "launches_per_step": 1}
+    del gc
 
     # ---------------- end to end: host buffers through the C ABI ----------------
     e2e = run_e2e(d, max(3, min(args.steps, 10)))
@@ -336,7 +352,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": d.name, "batch": d.batch, "buffer_length": d.buffer_length,
                    "kv_lora_rank": d.kv_lora_rank, "qk_rope_head_dim": d.rope_dim,
                    "n_out": d.n_out, "page_size": d.page_size, "num_pages": d.num_pages,
-                   "l2": "flushed before every timed step (256 MiB write, untimed)",
+                   "l2": "flushed before every timed step (256 MiB write, then 256 MiB read; untimed)",
                    "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
         "rows_per_s": whole_job_rate(rows * args.steps, world, t_max),
         "pct_tensor_peak": 100.0 * achieved / peaks["bf16_tflops"],

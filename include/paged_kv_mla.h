@@ -237,6 +237,45 @@ pkm_status mla_decompress_kv_paged_fp8(const pkm_paged_cache* cache, uint32_t la
                                        int32_t* dev_status, void* stream);
 
 /*
+ * The cache-write side of MLA: new latent rows are RMS-normalised and rotated, then
+ * stored into the paged latent cache.
+ * Source: mla_prefill_decode_graph_fp8 -- Args kv_input_fn ("load the KV latent values",
+ * [tot_seq_len, cache_head_dim]), kv_norm_gamma ("RMSNorm gamma weights for normalizing
+ * the KV cache", [kv_lora_rank]), epsilon ("Small constant for numerical stability in
+ * RMSNorm"), freqs_cis ("Precomputed RoPE frequency values for rotary position
+ * embeddings", [max_seq_len, qk_rope_head_dim]), input_row_offsets, kv_collection,
+ * layer_idx.
+ *
+ * For every request b and i < input_row_offsets[b+1] - input_row_offsets[b], with
+ * r = input_row_offsets[b] + i (r < total_rows) and position pos = cache_lengths[b] + i:
+ *     ms  = (sum_{k < R} x[r, k]^2) / R
+ *     slot(pos)[k]         = bf16( x[r, k] * kv_norm_gamma[k] / sqrt(ms + epsilon) ),  k < R
+ *     slot(pos)[R+2j, R+2j+1] = bf16( (x0 c - x1 s, x0 s + x1 c) ),  j < P/2,
+ *         (x0, x1) = x[r, R+2j .. R+2j+1],  (c, s) = freqs_cis[pos, 2j .. 2j+1]
+ * where slot(pos) is the cache row of layer_idx at page page_table[b][pos / page_size],
+ * slot pos % page_size.  fp32 arithmetic, round to nearest even.  No other cache element
+ * is written; cache_lengths are read, not updated.
+ *
+ *   latent          device bf16 [total_rows, R + P], row-major, 16-byte aligned.
+ *   input_row_offsets  device uint32 [batch+1], non-decreasing.
+ *   kv_lora_rank    R: a multiple of 8, at most 1024.
+ *   rope_dim        P: a multiple of 8, at most 256.
+ *   kv_norm_gamma   device fp32 [R], 16-byte aligned.
+ *   freqs_cis       device fp32 [max_seq_len, P], 16-byte aligned: P/2 (cos, sin) pairs
+ *                   per position (may be null when P = 0).
+ *   cache           row_elems = R + P; cache_lengths required.
+ * Errors: PKM_ERR_INVALID_ARG / PKM_ERR_UNSUPPORTED before any launch; a position past
+ * max_seq_len, the page-table row or the cache sets PKM_ERR_OUT_OF_RANGE in dev_status and
+ * leaves that row unwritten.
+ */
+pkm_status mla_cache_write_paged(const void* latent, const uint32_t* input_row_offsets,
+                                 int32_t batch, int32_t total_rows, int32_t kv_lora_rank,
+                                 int32_t rope_dim, const float* kv_norm_gamma, float epsilon,
+                                 const float* freqs_cis, int32_t max_seq_len,
+                                 const pkm_paged_cache* cache, uint32_t layer_idx,
+                                 int32_t* dev_status, void* stream);
+
+/*
  * FP8 decompress for callers that cannot allocate device memory.  The paper has no
  * counterpart: this entry point exists for users of this library, not for the method.
  *

@@ -71,6 +71,9 @@ _lib.mla_decompress_kv_paged_fp8.argtypes = [ctypes.POINTER(_CCache), _u32, _vp,
                                              _i32, _i32, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _vp,
                                              _vp, _vp, _vp, _sz, _vp, _vp]
 _lib.mla_decompress_kv_paged_fp8.restype = ctypes.c_int
+_lib.mla_cache_write_paged.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _vp, ctypes.c_float, _vp,
+                                       _i32, ctypes.POINTER(_CCache), _u32, _vp, _vp]
+_lib.mla_cache_write_paged.restype = ctypes.c_int
 _lib.kv_matmul_paged.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _i32, ctypes.POINTER(_CCache),
                                  _u32, _vp, _vp]
 _lib.kv_matmul_paged.restype = ctypes.c_int
@@ -220,6 +223,22 @@ def mla_decompress_kv_paged_fp8(cache: PagedCache, layer_idx: int,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
         _stream(stream))
     return _check(code, "mla_decompress_kv_paged_fp8", check)
+
+
+def mla_cache_write_paged(latent: torch.Tensor, input_row_offsets: torch.Tensor,
+                          kv_norm_gamma: torch.Tensor, epsilon: float, freqs_cis: torch.Tensor,
+                          cache: PagedCache, layer_idx: int, kv_lora_rank: int, rope_dim: int,
+                          dev_status: Optional[torch.Tensor] = None, stream=None,
+                          check: bool = True) -> int:
+    """RMSNorm + RoPE of new latent rows [total_rows, R + P] into the paged latent cache."""
+    c = cache.c_struct()
+    batch = int(input_row_offsets.shape[0]) - 1
+    code = _lib.mla_cache_write_paged(_ptr(latent), _ptr(input_row_offsets), batch,
+                                      int(latent.shape[0]), int(kv_lora_rank), int(rope_dim),
+                                      _ptr(kv_norm_gamma), float(epsilon), _ptr(freqs_cis),
+                                      int(freqs_cis.shape[0]), ctypes.byref(c), int(layer_idx),
+                                      _ptr(dev_status), _stream(stream))
+    return _check(code, "mla_cache_write_paged", check)
 
 
 def mla_decompress_k_paged_fp8_noalloc(cache: PagedCache, layer_idx: int,

@@ -16,6 +16,7 @@ namespace {
 
 using pkm::DecompressArgs;
 using pkm::Fp8Extra;
+using pkm::CacheWriteArgs;
 using pkm::KvMatmulArgs;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -438,6 +439,59 @@ pkm_status mla_decompress_kv_paged_fp8(const pkm_paged_cache* cache, uint32_t la
                           buffer_length, kv_lora_rank, rope_dim, w_k_e4m3, w_k_scale, n_out, v,
                           k_latent_buffer, k_buffer, workspace, workspace_bytes, dev_status,
                           stream);
+}
+
+pkm_status mla_cache_write_paged(const void* latent, const uint32_t* input_row_offsets,
+                                 int32_t batch, int32_t total_rows, int32_t kv_lora_rank,
+                                 int32_t rope_dim, const float* kv_norm_gamma, float epsilon,
+                                 const float* freqs_cis, int32_t max_seq_len,
+                                 const pkm_paged_cache* cache, uint32_t layer_idx,
+                                 int32_t* dev_status, void* stream) {
+    if (batch < 0 || total_rows < 0 || kv_lora_rank <= 0 || rope_dim < 0 || max_seq_len <= 0)
+        return PKM_ERR_INVALID_ARG;
+    if (batch == 0 || total_rows == 0) return PKM_OK;
+    if (latent == nullptr || input_row_offsets == nullptr || kv_norm_gamma == nullptr ||
+        (freqs_cis == nullptr && rope_dim > 0) || cache == nullptr || cache->data == nullptr ||
+        cache->page_table == nullptr || cache->cache_lengths == nullptr)
+        return PKM_ERR_INVALID_ARG;
+    if (cache->num_layers <= 0 || layer_idx >= static_cast<uint32_t>(cache->num_layers) ||
+        cache->num_pages <= 0 || cache->page_size <= 0 || cache->max_pages_per_seq <= 0)
+        return PKM_ERR_INVALID_ARG;
+    if (kv_lora_rank % 8 != 0 || kv_lora_rank > 1024 || rope_dim % 8 != 0 || rope_dim > 256)
+        return PKM_ERR_UNSUPPORTED;
+    if (cache->row_elems != kv_lora_rank + rope_dim) return PKM_ERR_INVALID_ARG;
+    if (!mult8(cache->layer_stride) || !mult8(cache->page_stride) || !mult8(cache->slot_stride))
+        return PKM_ERR_INVALID_ARG;
+    if (!aligned16(latent) || !aligned16(kv_norm_gamma) || !aligned16(freqs_cis) ||
+        !aligned16(cache->data) || !mult8(cache->layer_stride))
+        return PKM_ERR_INVALID_ARG;
+    CacheWriteArgs a{};
+    a.latent = static_cast<const uint16_t*>(latent);
+    a.row_offsets = input_row_offsets;
+    a.batch = batch;
+    a.total_rows = total_rows;
+    a.kv_lora_rank = kv_lora_rank;
+    a.rope_dim = rope_dim;
+    a.gamma = kv_norm_gamma;
+    a.epsilon = epsilon;
+    a.freqs = freqs_cis;
+    a.max_seq_len = max_seq_len;
+    a.cache_layer = static_cast<uint16_t*>(cache->data) +
+                    static_cast<int64_t>(layer_idx) * cache->layer_stride;
+    a.page_stride = cache->page_stride;
+    a.slot_stride = cache->slot_stride;
+    a.num_pages = cache->num_pages;
+    a.page_size = cache->page_size;
+    a.max_pages = cache->max_pages_per_seq;
+    a.page_table = cache->page_table;
+    a.cache_lengths = cache->cache_lengths;
+    a.status = dev_status;
+    a.timeout_ns = wait_timeout_ns();
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
+    return pkm::launch_cache_write(a, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKM_OK
+               : PKM_ERR_CUDA;
 }
 
 pkm_status kv_matmul_paged(const void* hidden_state, const uint32_t* input_row_offsets,

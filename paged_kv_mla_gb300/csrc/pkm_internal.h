@@ -47,6 +47,27 @@ struct Fp8Extra {
     const float* w_scale_v;        // [N_v/128, R/128], or null
 };
 
+// One cache write (new latent rows -> RMSNorm / RoPE -> paged latent cache), validated.
+struct CacheWriteArgs {
+    const uint16_t* latent;        // [total_rows, R + P] bf16
+    const uint32_t* row_offsets;   // input_row_offsets [batch + 1]
+    int32_t batch;
+    int32_t total_rows;
+    int32_t kv_lora_rank;          // R, multiple of 8, <= 1024
+    int32_t rope_dim;              // P, multiple of 8, <= 256
+    const float* gamma;            // [R]
+    float epsilon;
+    const float* freqs;            // [max_seq_len, P]
+    int32_t max_seq_len;
+    uint16_t* cache_layer;         // cache data + layer_idx * layer_stride
+    int64_t page_stride, slot_stride;
+    int32_t num_pages, page_size, max_pages;
+    const uint32_t* page_table;
+    const uint32_t* cache_lengths;
+    int32_t* status;
+    uint64_t timeout_ns;
+};
+
 // One kv_matmul problem, already validated.
 struct KvMatmulArgs {
     const uint16_t* hidden;        // [M, K] bf16
@@ -79,6 +100,7 @@ cudaError_t launch_decompress_fp8_gemm(const CUtensorMap& tm_q, const CUtensorMa
                                        Fp8Extra extra, int num_sms, cudaStream_t stream);
 cudaError_t launch_kv_matmul(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                              KvMatmulArgs args, int num_sms, cudaStream_t stream);
+cudaError_t launch_cache_write(CacheWriteArgs args, int num_sms, cudaStream_t stream);
 cudaError_t launch_wait_timeout_check(int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 
 // Row bookkeeping shared by the decompress kernels: element offset (inside the layer) of

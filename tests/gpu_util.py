@@ -6,7 +6,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from workloads import SENTINEL_OUT, DecompressInputs, KvMatmulInputs
+from workloads import SENTINEL_OUT, CacheWriteInputs, DecompressInputs, KvMatmulInputs
 
 BF16_TOL = (1e-2, 2e-3)   # |gpu - ref| <= rtol * |ref| + atol, bf16 in / fp32 accumulate
 FP8_TOL = (3e-2, 5e-3)    # same form, FP8 path against the dequantised-value oracle
@@ -150,3 +150,33 @@ class DeviceKvMatmul:
     def results(self):
         torch.cuda.synchronize()
         return host_u16(self.cache).reshape(self.k.cache.shape), int(self.status.item())
+
+
+class DeviceCacheWrite:
+    def __init__(self, c: CacheWriteInputs):
+        import paged_kv_mla_gb300 as pkm
+        self.c = c
+        self.latent = dev(c.latent)
+        self.iro = dev(c.input_row_offsets)
+        self.gamma = torch.from_numpy(c.gamma).cuda()
+        self.freqs = torch.from_numpy(np.ascontiguousarray(c.freqs_cis)).cuda()
+        self.cache = dev(c.cache)
+        self.pt = dev(c.page_table)
+        self.cl = dev(c.cache_lengths)
+        ls, ps, ss = c.strides
+        self.pc = pkm.PagedCache(data=self.cache, page_table=self.pt, layer_stride=ls,
+                                 page_stride=ps, slot_stride=ss, num_layers=c.cache.shape[0],
+                                 num_pages=c.num_pages, page_size=c.page_size,
+                                 row_elems=c.row_elems, cache_lengths=self.cl)
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def run(self, stream=None, check=True):
+        import paged_kv_mla_gb300 as pkm
+        c = self.c
+        return pkm.mla_cache_write_paged(self.latent, self.iro, self.gamma, c.epsilon, self.freqs,
+                                         self.pc, c.layer_idx, c.kv_lora_rank, c.rope_dim,
+                                         dev_status=self.status, stream=stream, check=check)
+
+    def results(self):
+        torch.cuda.synchronize()
+        return host_u16(self.cache).reshape(self.c.cache.shape), int(self.status.item())

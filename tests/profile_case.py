@@ -19,7 +19,7 @@ sys.path.insert(0, HERE)
 def main():
     import torch
     import workloads
-    from gpu_util import DeviceDecompress, DeviceKvMatmul
+    from gpu_util import DeviceCacheWrite, DeviceDecompress, DeviceKvMatmul
 
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default="deepseek_v3_bf16_decompress",
@@ -29,6 +29,8 @@ def main():
     w = workloads.WORKLOADS[args.workload]()
     if args.workload == "kv_matmul_write_path":
         g = DeviceKvMatmul(w)
+    elif args.workload == "cache_write_path":
+        g = DeviceCacheWrite(w)
     else:
         g = DeviceDecompress(w, fp8=w.w_k_e4m3 is not None)
     for _ in range(args.launches):

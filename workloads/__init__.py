@@ -295,9 +295,10 @@ class CacheWriteInputs:
 
     @property
     def bytes_moved(self) -> int:
-        """Algorithmic HBM bytes: read every new row, write it into the cache (bf16)."""
+        """Algorithmic HBM bytes: read every new row and write it into the cache (bf16), read
+        gamma and the freqs_cis table once."""
         rows = int(self.input_row_offsets[-1])
-        return 2 * rows * self.row_elems * 2
+        return 2 * rows * self.row_elems * 2 + self.gamma.nbytes + self.freqs_cis.nbytes
 
 
 def make_cache_write(name, seed, new_tokens, cache_lengths, kv_lora_rank, rope_dim, page_size,
