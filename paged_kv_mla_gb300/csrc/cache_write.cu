@@ -13,11 +13,12 @@
 //
 // A streaming kernel, HBM-bound (2 x 1152 bytes a row for DeepSeek-V3 shapes).  One
 // persistent CTA per SM owns a contiguous range of rows, taken 30 at a time (a chunk)
-// through a ring of shared-memory stages.  The producer warp fills a stage without ever
-// waiting on a global load: lane 0 bulk-copies the chunk's rows, and lane i < 30 resolves
-// row i's position (its request only moves forward, so the offsets and cache lengths are
-// re-read once per request), bulk-copies that position's freqs_cis row and fetches the
-// row's page id with a 4-byte cp.async, all completing on the stage's barrier.  Each of 15
+// through a ring of shared-memory stages.  In the producer warp lane i < 30 resolves row i's
+// position (its request only moves forward, so the offsets and cache lengths are re-read
+// once per request) and loads its page id while the stage is still in use; once the stage
+// is free the lanes write slots and page ids into it, each run of rows of one request
+// bulk-copies its (consecutive) freqs_cis rows, lane 0 bulk-copies the chunk's rows, and
+// all of it completes on the stage's barrier.  Each of 15
 // consumer warps then takes two rows of the chunk out of shared memory, frees the stage,
 // reduces the sum of squares across the warp and writes the normalised and rotated rows
 // (fp32 arithmetic, rounded to bf16) straight into their slots with 16-byte stores.
@@ -89,6 +90,12 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
     }
 }
 
+// Bytes of latent rows in the chunk starting at row r0.
+__device__ __forceinline__ uint32_t rows_bytes_of(int64_t r0, int64_t total_rows, int C) {
+    const int64_t rows = min(static_cast<int64_t>(kChunkRows), total_rows - r0);
+    return static_cast<uint32_t>(rows * C * 2);
+}
+
 // NC = 16-byte chunks of the normalised part per lane (ceil(R / 256)).
 template <int NC>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -103,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t c_end = n_chunks * (blockIdx.x + 1) / gridDim.x;
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
-            mbar_init(&bars.full[s], 32);  // every producer lane arrives
+            mbar_init(&bars.full[s], 1);  // producer lane 0, with the stage's byte count
             mbar_init(&bars.empty[s], kConsumerWarps);
         }
         bars.abort_flag = 0;
@@ -119,43 +126,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         RowCursor q;
         q.init(a, c_begin * kChunkRows + lane);
         for (int64_t k = c_begin; k < c_end; ++k) {
+            // lane i < 30: row i of the chunk -> slot and page id (loaded before the stage is
+            // free, so that the load overlaps the wait)
+            const int64_t r0 = k * kChunkRows;
+            const int64_t r = r0 + lane;
+            int32_t slot = kSlotNone, req = -1;
+            uint32_t page = 0;
+            uint64_t pos = 0;
+            if (lane < kChunkRows && r < covered && q.seek(a, r)) {
+                pos = static_cast<uint64_t>(q.cl) + static_cast<uint64_t>(r - q.lo);
+                const uint64_t lp = pos / static_cast<uint64_t>(a.page_size);
+                if (pos >= static_cast<uint64_t>(a.max_seq_len) ||
+                    lp >= static_cast<uint64_t>(a.max_pages)) {
+                    slot = kSlotOutOfRange;
+                } else {
+                    slot = static_cast<int32_t>(pos % static_cast<uint64_t>(a.page_size));
+                    page = __ldg(a.page_table + static_cast<int64_t>(q.b) * a.max_pages + lp);
+                    req = q.b;
+                }
+            }
             int ok = 1;
             if (lane == 0) ok = mbar_wait(&bars.empty[p.stage], p.phase ^ 1u, wc);
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             __syncwarp();  // the consumers' reads of this stage precede every lane's writes
             uint8_t* stage = smem + p.stage * L.bytes;
             uint64_t* full = &bars.full[p.stage];
-            const int64_t r0 = k * kChunkRows;
-            if (lane == 0) {
-                const int64_t rows = min(static_cast<int64_t>(kChunkRows), a.total_rows - r0);
-                const uint32_t bytes = static_cast<uint32_t>(rows * C * 2);
-                mbar_expect_tx(full, bytes);
-                bulk_load_1d(stage, a.latent + r0 * C, bytes, full);
-            }
             if (lane < kChunkRows) {
-                const int64_t r = r0 + lane;
-                int32_t slot = kSlotNone;
-                if (r < covered && q.seek(a, r)) {
-                    const uint64_t pos = static_cast<uint64_t>(q.cl) + static_cast<uint64_t>(r - q.lo);
-                    const uint64_t lp = pos / static_cast<uint64_t>(a.page_size);
-                    if (pos >= static_cast<uint64_t>(a.max_seq_len) ||
-                        lp >= static_cast<uint64_t>(a.max_pages)) {
-                        slot = kSlotOutOfRange;
-                    } else {
-                        slot = static_cast<int32_t>(pos % static_cast<uint64_t>(a.page_size));
-                        cp_async_4(smem_u32(stage + L.page + lane * 4),
-                                   a.page_table + static_cast<int64_t>(q.b) * a.max_pages + lp);
-                        if (P > 0) {
-                            mbar_expect_tx(full, static_cast<uint32_t>(P * 4));
-                            bulk_load_1d(stage + L.freqs + lane * P * 4, a.freqs + pos * P,
-                                         static_cast<uint32_t>(P * 4), full);
-                        }
-                    }
-                }
                 reinterpret_cast<int32_t*>(stage + L.slot)[lane] = slot;
+                reinterpret_cast<uint32_t*>(stage + L.page)[lane] = page;
             }
-            cp_async_mbar_arrive(full);  // the page id lands before the phase completes
-            mbar_arrive(full);
+            // freqs_cis rows: one bulk copy per run of rows of one request (consecutive
+            // positions, so consecutive freqs_cis rows)
+            const bool live = slot >= 0;
+            const int prev_live = __shfl_up_sync(0xffffffffu, live ? 1 : 0, 1);
+            const int prev_req = __shfl_up_sync(0xffffffffu, req, 1);
+            const bool run_start = live && (lane == 0 || !prev_live || prev_req != req);
+            const uint32_t live_mask = __ballot_sync(0xffffffffu, live);
+            const uint32_t bound = __ballot_sync(0xffffffffu, !live || run_start);
+            if (run_start && P > 0) {
+                const uint32_t after = bound & ~((2u << lane) - 1u);  // lane < 30 here
+                const int len = __ffs(after) - 1 - lane;
+                bulk_load_1d(stage + L.freqs + lane * P * 4, a.freqs + pos * P,
+                             static_cast<uint32_t>(len * P * 4), full);
+            }
+            if (lane == 0)
+                bulk_load_1d(stage, a.latent + r0 * C, rows_bytes_of(r0, a.total_rows, C), full);
+            __syncwarp();  // slots and page ids are written before lane 0 releases them
+            if (lane == 0)
+                mbar_arrive_expect_tx(full, rows_bytes_of(r0, a.total_rows, C) +
+                                                static_cast<uint32_t>(__popc(live_mask) * P * 4));
             p.next(stages);
         }
     } else {
