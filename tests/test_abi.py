@@ -33,7 +33,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ["mla_decompress_k_paged", "mla_decompress_k_paged_fp8", "mla_decompress_kv_paged",
-              "mla_decompress_kv_paged_fp8",
+              "mla_decompress_kv_paged_fp8", "mla_cache_write_paged",
               "mla_decompress_k_paged_fp8_workspace_size", "kv_matmul_paged", "pkm_status_string"]:
         assert n in names
 
@@ -108,6 +108,22 @@ def test_invalid_calls_return_status_without_a_gpu(lib):
     assert call_kv(wv) == pkm.PKM_ERR_UNSUPPORTED                      # H * Dv not a multiple of 64
     assert call_kv(torch.zeros(1, 64, 64, dtype=torch.int16), v=t16[1:]) == pkm.PKM_ERR_INVALID_ARG  # misaligned v
     assert call_kv(wv, L=0) == pkm.PKM_OK                              # nothing to do
+    # cache write: shapes, alignment and the cache descriptor are checked before any launch
+    lat = torch.zeros(4, 80, dtype=torch.int16)
+    gamma = torch.ones(64, dtype=torch.float32)
+    freqs = torch.zeros(32, 16, dtype=torch.float32)
+    cw_cache = _cache(pkm, cache_lengths=co)
+
+    def call_cw(cache=cw_cache, lat=lat, R=64, P=16, gamma=gamma, freqs=freqs, iro=bro):
+        return pkm.mla_cache_write_paged(lat, iro, gamma, 1e-6, freqs, cache, 0, R, P, stream=0,
+                                         check=False)
+    assert call_cw(R=60, P=20) == pkm.PKM_ERR_UNSUPPORTED               # R not a multiple of 8
+    assert call_cw(R=1032, P=16) == pkm.PKM_ERR_UNSUPPORTED             # R above 1024
+    assert call_cw(R=56, P=16) == pkm.PKM_ERR_INVALID_ARG               # row_elems != R + P
+    assert call_cw(cache=_cache(pkm)) == pkm.PKM_ERR_INVALID_ARG        # cache_lengths missing
+    assert call_cw(gamma=torch.ones(65, dtype=torch.float32)[1:]) == pkm.PKM_ERR_INVALID_ARG  # misaligned gamma
+    assert call_cw(cache=_cache(pkm, cache_lengths=co, slot_stride=81)) == pkm.PKM_ERR_INVALID_ARG
+    assert call_cw(lat=lat[:0]) == pkm.PKM_OK                           # no new rows
 
 
 def test_oracle_and_product_share_no_code():
