@@ -10,9 +10,9 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 import workloads
 from gpu_util import BF16_TOL, DeviceCacheWrite, assert_close_bf16
+from util import oracle_cache_write
 
 pytestmark = pytest.mark.gpu
 
@@ -24,21 +24,11 @@ def _gpu():
     import paged_kv_mla_gb300  # noqa: F401  (raises if the library is missing)
 
 
-def oracle_run(c: workloads.CacheWriteInputs):
-    ls, ps, ss = c.strides
-    v = oracle.PagedCacheView(c.cache.copy(), ls, ps, ss, c.num_pages, c.page_size,
-                              c.page_table, c.page_table.shape[1])
-    st = oracle.cache_write(c.latent, c.input_row_offsets, c.batch, c.total_rows, c.kv_lora_rank,
-                            c.rope_dim, c.gamma, c.epsilon, c.freqs_cis, v, c.cache_lengths,
-                            c.layer_idx)
-    return st, v.data.reshape(c.cache.shape)
-
-
 def check_full(c, expect_status=0):
     g = DeviceCacheWrite(c)
     g.run()
     out, status = g.results()
-    st, ref = oracle_run(c)
+    st, ref = oracle_cache_write(c)
     assert st == expect_status and status == expect_status
     changed_ref = ref != c.cache
     changed_gpu = out != c.cache
@@ -82,7 +72,7 @@ def test_cache_write_exact_inputs_bit_exact():
     gpu = DeviceCacheWrite(c)
     gpu.run()
     out, status = gpu.results()
-    st, ref = oracle_run(c)
+    st, ref = oracle_cache_write(c)
     assert status == 0 and st == 0
     assert np.array_equal(out, ref)
 
@@ -113,7 +103,7 @@ def test_cache_write_empty_and_stream():
         g.run(stream=s)
     s.synchronize()
     out, status = g.results()
-    st, ref = oracle_run(c)
+    st, ref = oracle_cache_write(c)
     changed = ref != c.cache
     assert status == 0 and np.array_equal(changed, out != c.cache)
     assert_close_bf16(out[changed], ref[changed], BF16_TOL, "cache values")

@@ -5,7 +5,7 @@ from __future__ import annotations
 import numpy as np
 
 import oracle
-from workloads import DecompressInputs, KvMatmulInputs
+from workloads import CacheWriteInputs, DecompressInputs, KvMatmulInputs
 
 
 def f32_to_bf16_exact(a) -> np.ndarray:
@@ -71,6 +71,17 @@ def oracle_kv_matmul(k: KvMatmulInputs):
     st = oracle.kv_matmul(k.hidden_state, k.input_row_offsets, k.batch, k.total_rows, k.weight,
                           view, k.head_elems, k.cache_lengths, k.layer_idx)
     return st, view.data.reshape(k.cache.shape)
+
+
+def oracle_cache_write(c: CacheWriteInputs):
+    """Runs the cache-write oracle on a copy of the cache; returns (status, cache_after)."""
+    ls, ps, ss = c.strides
+    view = oracle.PagedCacheView(c.cache.copy(), ls, ps, ss, c.num_pages, c.page_size,
+                                 c.page_table, c.page_table.shape[1])
+    st = oracle.cache_write(c.latent, c.input_row_offsets, c.batch, c.total_rows, c.kv_lora_rank,
+                            c.rope_dim, c.gamma, c.epsilon, c.freqs_cis, view, c.cache_lengths,
+                            c.layer_idx)
+    return st, view.data.reshape(c.cache.shape)
 
 
 def e4m3_decode_table() -> np.ndarray:
