@@ -11,6 +11,8 @@ Each wrapper follows the passage cited in the C source:
     w_uv, w_uv_scale)
   * mla_prefill_decode_graph_fp8 -- Args kv_input_fn, kv_norm_gamma, epsilon, freqs_cis
     (the cache-write side)
+  * PagedKVCacheCollection[..., scale_dtype_, quantization_granularity_] -- the quantised
+    paged latent cache (written by the cache-write side, read by the FP8 decompress)
   * kv_matmul_ragged_paged -- Args (hidden_state, input_row_offsets, weight, kv_collection)
 """
 from __future__ import annotations
@@ -99,6 +101,23 @@ def lib():
                                              _f32p, _i32, _u16p, _i64, _i64, _i64, _i32, _i32, _u32p,
                                              _i32, _u32p, _u32]
             L.oracle_cache_write.restype = ctypes.c_int
+            qcache_args = [_u8p, _i64, _i64, _i64, _i32, _i32, _u32p, _i32, _u32, _u32p, _u32p,
+                           _i32, _i32]
+            L.oracle_dequant_bf16.argtypes = [ctypes.c_uint8, ctypes.c_float]
+            L.oracle_dequant_bf16.restype = ctypes.c_uint16
+            L.oracle_qslot_bytes.argtypes = [_i32, _i32]
+            L.oracle_qslot_bytes.restype = ctypes.c_int64
+            L.oracle_cache_write_q.argtypes = [_u16p, _u32p, _i32, _i32, _i32, _i32, _f32p,
+                                               ctypes.c_float, _f32p, _i32, _u8p, _i64, _i64, _i64,
+                                               _i32, _i32, _u32p, _i32, _u32p, _u32]
+            L.oracle_cache_write_q.restype = ctypes.c_int
+            L.oracle_decompress_k_qcache_fp8.argtypes = qcache_args + [_i32, _i32, _u8p, _f32p, _i32,
+                                                                       _u16p, _u16p, _u8p, _f32p, _u8p]
+            L.oracle_decompress_k_qcache_fp8.restype = ctypes.c_int
+            L.oracle_decompress_k_qcache_fp8_row.argtypes = qcache_args + [_i32, _i32, _u8p, _f32p,
+                                                                           _i32, _i64, _u16p, _u16p,
+                                                                           _u8p, _f32p]
+            L.oracle_decompress_k_qcache_fp8_row.restype = ctypes.c_int
             L.oracle_kv_matmul.argtypes = [_u16p, _u32p, _i32, _i32, _i32, _u16p, _i32, _u16p, _i64,
                                            _i64, _i64, _i64, _i32, _i32, _i32, _u32p, _i32, _u32p,
                                            _u32]
@@ -377,6 +396,91 @@ def cache_write(latent, input_row_offsets, batch, total_rows, kv_lora_rank, rope
                                     cache.page_stride, cache.slot_stride, cache.num_pages,
                                     cache.page_size, cache.page_table, cache.max_pages_per_seq,
                                     _c(cache_lengths, np.uint32), int(layer_idx))
+
+
+class QuantCacheView:
+    """Host view of one quantised paged latent cache: flat bytes plus byte strides (slot
+    layout in pkm_oracle.c: codes, rope bf16, fp32 block scales)."""
+
+    def __init__(self, data, layer_stride, page_stride, slot_stride, num_pages, page_size,
+                 page_table, max_pages_per_seq):
+        self.data = _c(np.asarray(data).reshape(-1), np.uint8)
+        self.layer_stride = int(layer_stride)
+        self.page_stride = int(page_stride)
+        self.slot_stride = int(slot_stride)
+        self.num_pages = int(num_pages)
+        self.page_size = int(page_size)
+        self.page_table = _c(np.asarray(page_table).reshape(-1), np.uint32)
+        self.max_pages_per_seq = int(max_pages_per_seq)
+
+    def args(self, layer_idx, bro, co, batch, buffer_length):
+        return [self.data, self.layer_stride, self.page_stride, self.slot_stride, self.num_pages,
+                self.page_size, self.page_table, self.max_pages_per_seq, int(layer_idx),
+                _c(bro, np.uint32), _c(co, np.uint32), int(batch), int(buffer_length)]
+
+
+def dequant_bf16(code: int, scale: float) -> int:
+    return int(lib().oracle_dequant_bf16(int(code), float(np.float32(scale))))
+
+
+def qslot_bytes(kv_lora_rank, rope_dim) -> int:
+    return int(lib().oracle_qslot_bytes(int(kv_lora_rank), int(rope_dim)))
+
+
+def cache_write_q(latent, input_row_offsets, batch, total_rows, kv_lora_rank, rope_dim, gamma,
+                  epsilon, freqs_cis, cache: QuantCacheView, cache_lengths, layer_idx):
+    """RMSNorm + RoPE of new latent rows, quantised into the paged cache's slots; cache.data
+    is modified in place.  Returns the status."""
+    freqs_cis = _c(freqs_cis, np.float32)
+    return lib().oracle_cache_write_q(_c(latent, np.uint16).reshape(-1), _c(input_row_offsets, np.uint32),
+                                      int(batch), int(total_rows), int(kv_lora_rank), int(rope_dim),
+                                      _c(gamma, np.float32), float(epsilon), freqs_cis.reshape(-1),
+                                      int(freqs_cis.shape[0]), cache.data, cache.layer_stride,
+                                      cache.page_stride, cache.slot_stride, cache.num_pages,
+                                      cache.page_size, cache.page_table, cache.max_pages_per_seq,
+                                      _c(cache_lengths, np.uint32), int(layer_idx))
+
+
+def decompress_k_qcache_fp8(cache: QuantCacheView, layer_idx, bro, co, batch, buffer_length,
+                            kv_lora_rank, rope_dim, w_e4m3, w_scale, k_latent=None, k_buffer=None):
+    """FP8 decompress from a quantised cache.  Returns (status, k_latent, k_buffer, q_latent,
+    q_scale, row_written)."""
+    w_e4m3 = _c(w_e4m3, np.uint8)
+    w_scale = _c(w_scale, np.float32)
+    n_out = w_e4m3.shape[0]
+    C = kv_lora_rank + rope_dim
+    L1 = max(buffer_length, 1)
+    if k_latent is None:
+        k_latent = np.zeros((L1, C), np.uint16)
+    if k_buffer is None:
+        k_buffer = np.zeros((L1, n_out), np.uint16)
+    q = np.zeros((L1, kv_lora_rank), np.uint8)
+    qs = np.zeros((L1, kv_lora_rank // 128), np.float32)
+    written = np.zeros(L1, np.uint8)
+    st = lib().oracle_decompress_k_qcache_fp8(*cache.args(layer_idx, bro, co, batch, buffer_length),
+                                              kv_lora_rank, rope_dim, w_e4m3.reshape(-1),
+                                              w_scale.reshape(-1), n_out, k_latent.reshape(-1),
+                                              k_buffer.reshape(-1), q.reshape(-1), qs.reshape(-1),
+                                              written)
+    L = buffer_length
+    return st, k_latent[:L], k_buffer[:L], q[:L], qs[:L], written[:L].astype(bool)
+
+
+def decompress_k_qcache_fp8_row(cache: QuantCacheView, layer_idx, bro, co, batch, buffer_length,
+                                kv_lora_rank, rope_dim, w_e4m3, w_scale, r):
+    """One row of the quantised-cache FP8 decompress.  Returns (status, latent_row, k_row,
+    q_row, scale_row)."""
+    w_e4m3 = _c(w_e4m3, np.uint8)
+    n_out = w_e4m3.shape[0]
+    lat = np.zeros(kv_lora_rank + rope_dim, np.uint16)
+    k = np.zeros(n_out, np.uint16)
+    q = np.zeros(kv_lora_rank, np.uint8)
+    s = np.zeros(kv_lora_rank // 128, np.float32)
+    st = lib().oracle_decompress_k_qcache_fp8_row(*cache.args(layer_idx, bro, co, batch, buffer_length),
+                                                  kv_lora_rank, rope_dim, w_e4m3.reshape(-1),
+                                                  _c(w_scale, np.float32).reshape(-1), n_out, int(r),
+                                                  lat, k, q, s)
+    return st, lat, k, q, s
 
 
 def kv_matmul(hidden_state, input_row_offsets, batch, total_rows, weight, cache: PagedCacheView,

@@ -20,6 +20,9 @@
  *     gathered latent rows (bf16 and block-scaled FP8).
  *   - mla_prefill_decode_graph_fp8, Args kv_input_fn, kv_norm_gamma, epsilon, freqs_cis: the
  *     cache-write side (RMSNorm and RoPE of new latent rows, stored into the paged cache).
+ *   - PagedKVCacheCollection's type parameters scale_dtype_ and quantization_granularity_
+ *     (generic_flare_mla_decompress_k_cache_ragged_paged, signature): a quantised paged
+ *     latent cache, written by the cache-write side and read by the FP8 decompress.
  *   - kv_matmul_ragged_paged (Modular MAX kernels, nn/kv_cache_ragged), Args: a GEMM on
  *     the ragged hidden_state whose rows are written into the paged cache of one layer,
  *     after each request's existing cache length.
@@ -576,6 +579,26 @@ int oracle_decompress_kv_fp8_row(const uint16_t* cache, int64_t layer_stride,
  * Nothing else in the cache is written.  Returns 0, or 4 if a row's position resolves
  * outside the page table / the cache or past max_seq_len (that row is skipped).
  */
+/* One row: x (R + P bf16 values) -> y, with f = freqs_cis[pos]. */
+static void cache_write_row(const uint16_t* x, int32_t kv_lora_rank, int32_t rope_dim,
+                            const float* gamma, float epsilon, const float* f, uint16_t* y) {
+    double sumsq = 0.0;
+    for (int32_t k = 0; k < kv_lora_rank; ++k) {
+        double v = oracle_bf16_to_double(x[k]);
+        sumsq += v * v;
+    }
+    double inv = 1.0 / sqrt(sumsq / (double)kv_lora_rank + (double)epsilon);
+    for (int32_t k = 0; k < kv_lora_rank; ++k)
+        y[k] = oracle_double_to_bf16(oracle_bf16_to_double(x[k]) * inv * (double)gamma[k]);
+    for (int32_t j = 0; j < rope_dim / 2; ++j) {
+        double x0 = oracle_bf16_to_double(x[kv_lora_rank + 2 * j]);
+        double x1 = oracle_bf16_to_double(x[kv_lora_rank + 2 * j + 1]);
+        double c = (double)f[2 * j], sn = (double)f[2 * j + 1];
+        y[kv_lora_rank + 2 * j] = oracle_double_to_bf16(x0 * c - x1 * sn);
+        y[kv_lora_rank + 2 * j + 1] = oracle_double_to_bf16(x0 * sn + x1 * c);
+    }
+}
+
 int oracle_cache_write(const uint16_t* latent, const uint32_t* input_row_offsets,
                        int32_t batch, int32_t total_rows, int32_t kv_lora_rank,
                        int32_t rope_dim, const float* gamma, float epsilon,
@@ -600,27 +623,174 @@ int oracle_cache_write(const uint16_t* latent, const uint32_t* input_row_offsets
                 status = 4;
                 continue;
             }
-            const uint16_t* x = latent + r * (uint64_t)C;
-            uint16_t* y = layer + off;
-            double sumsq = 0.0;
-            for (int32_t k = 0; k < kv_lora_rank; ++k) {
-                double v = oracle_bf16_to_double(x[k]);
-                sumsq += v * v;
-            }
-            double inv = 1.0 / sqrt(sumsq / (double)kv_lora_rank + (double)epsilon);
-            for (int32_t k = 0; k < kv_lora_rank; ++k)
-                y[k] = oracle_double_to_bf16(oracle_bf16_to_double(x[k]) * inv * (double)gamma[k]);
-            const float* f = freqs_cis + pos * (uint64_t)rope_dim;
-            for (int32_t j = 0; j < rope_dim / 2; ++j) {
-                double x0 = oracle_bf16_to_double(x[kv_lora_rank + 2 * j]);
-                double x1 = oracle_bf16_to_double(x[kv_lora_rank + 2 * j + 1]);
-                double c = (double)f[2 * j], sn = (double)f[2 * j + 1];
-                y[kv_lora_rank + 2 * j] = oracle_double_to_bf16(x0 * c - x1 * sn);
-                y[kv_lora_rank + 2 * j + 1] = oracle_double_to_bf16(x0 * sn + x1 * c);
-            }
+            cache_write_row(latent + r * (uint64_t)C, kv_lora_rank, rope_dim, gamma, epsilon,
+                            freqs_cis + pos * (uint64_t)rope_dim, layer + off);
         }
     }
     return status;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Quantised paged latent cache (PagedKVCacheCollection scale_dtype_,                    */
+/* quantization_granularity_)                                                            */
+/* ------------------------------------------------------------------------------------ */
+
+/*
+ * The collection's type parameters scale_dtype_ and quantization_granularity_ say that a
+ * paged cache may hold quantised values with scales; the pages give no layout and no rule.
+ * Readings:
+ *   - one token's slot is a byte string:
+ *         [0, R)                     e4m3 codes of the R nope columns,
+ *         [R, R + 2P)                the P rope columns in bf16 (not quantised),
+ *         [R + 2P, R + 2P + 4R/128)  fp32 scales, one per 128-column block
+ *     (scale_dtype_ = float32, quantization_granularity_ = 128 columns of one token);
+ *   - the codes and scales are exactly what the FP8 decompress's activation quantisation
+ *     (oracle_quantize_row_e4m3) makes of the bf16 row the bf16 cache would hold, so a
+ *     quantised cache feeds the block-scaled product the same operands;
+ *   - a nope value reads back as fl32(dq(code) * scale) rounded to bf16: the dequantisation
+ *     is taken in the scale's dtype.
+ * Strides of a quantised cache are in bytes.
+ */
+
+uint16_t oracle_dequant_bf16(uint8_t code, float scale) {
+    volatile float p = (float)oracle_e4m3_to_double(code) * scale;  /* one fp32 rounding */
+    return oracle_double_to_bf16((double)p);
+}
+
+/* Stores the bf16 row y (R + P values) into a quantised slot. */
+static void qslot_store(const uint16_t* y, int32_t kv_lora_rank, int32_t rope_dim,
+                        uint8_t* slot) {
+    float scales[8];
+    oracle_quantize_row_e4m3(y, kv_lora_rank, slot, scales);
+    memcpy(slot + kv_lora_rank, y + kv_lora_rank, sizeof(uint16_t) * (size_t)rope_dim);
+    memcpy(slot + kv_lora_rank + 2 * rope_dim, scales, sizeof(float) * (size_t)(kv_lora_rank / 128));
+}
+
+/* Bytes of a quantised slot's payload (its stride may be larger). */
+int64_t oracle_qslot_bytes(int32_t kv_lora_rank, int32_t rope_dim) {
+    return (int64_t)kv_lora_rank + 2 * (int64_t)rope_dim + 4 * (int64_t)(kv_lora_rank / 128);
+}
+
+/*
+ * Cache write into a quantised cache: the row oracle_cache_write would store (RMSNorm,
+ * RoPE, bf16), quantised into the slot as above.  R is a multiple of 128, at most 1024;
+ * P at most 256.  Same positions, same status as oracle_cache_write.
+ */
+int oracle_cache_write_q(const uint16_t* latent, const uint32_t* input_row_offsets,
+                         int32_t batch, int32_t total_rows, int32_t kv_lora_rank,
+                         int32_t rope_dim, const float* gamma, float epsilon,
+                         const float* freqs_cis, int32_t max_seq_len, uint8_t* cache,
+                         int64_t layer_stride, int64_t page_stride, int64_t slot_stride,
+                         int32_t num_pages, int32_t page_size, const uint32_t* page_table,
+                         int32_t max_pages_per_seq, const uint32_t* cache_lengths,
+                         uint32_t layer_idx) {
+    int status = 0;
+    const int32_t C = kv_lora_rank + rope_dim;
+    uint16_t y[1280];
+    uint8_t* layer = cache + (int64_t)layer_idx * layer_stride;
+    for (int32_t b = 0; b < batch; ++b) {
+        uint32_t begin = input_row_offsets[b];
+        uint32_t end = input_row_offsets[b + 1];
+        for (uint32_t i = 0; begin + i < end; ++i) {
+            uint64_t r = (uint64_t)begin + i;
+            if (r >= (uint64_t)total_rows) break;
+            uint64_t pos = (uint64_t)cache_lengths[b] + i;
+            int64_t off = token_offset(page_table, max_pages_per_seq, num_pages, page_size,
+                                       page_stride, slot_stride, b, pos);
+            if (off < 0 || pos >= (uint64_t)max_seq_len) {
+                status = 4;
+                continue;
+            }
+            cache_write_row(latent + r * (uint64_t)C, kv_lora_rank, rope_dim, gamma, epsilon,
+                            freqs_cis + pos * (uint64_t)rope_dim, y);
+            qslot_store(y, kv_lora_rank, rope_dim, layer + off);
+        }
+    }
+    return status;
+}
+
+/* Reads one quantised slot: codes and scales as stored, the bf16 latent row dequantised. */
+static void qslot_load(const uint8_t* slot, int32_t kv_lora_rank, int32_t rope_dim,
+                       uint16_t* latent_row, uint8_t* q_row, float* scale_row) {
+    memcpy(q_row, slot, (size_t)kv_lora_rank);
+    memcpy(scale_row, slot + kv_lora_rank + 2 * rope_dim,
+           sizeof(float) * (size_t)(kv_lora_rank / 128));
+    for (int32_t k = 0; k < kv_lora_rank; ++k)
+        latent_row[k] = oracle_dequant_bf16(q_row[k], scale_row[k / 128]);
+    memcpy(latent_row + kv_lora_rank, slot + kv_lora_rank, sizeof(uint16_t) * (size_t)rope_dim);
+}
+
+/*
+ * FP8 decompress from a quantised cache: the rows and tokens of the decompress; each
+ * written row takes its slot's codes and scales as they are (q_latent, q_scale), its
+ * dequantised bf16 row (k_latent, C = R + P columns) and the block-scaled product with
+ * the e4m3 weight (k_buffer).  Returns 0, or 4 as the gather does.
+ */
+int oracle_decompress_k_qcache_fp8(const uint8_t* cache, int64_t layer_stride,
+                                   int64_t page_stride, int64_t slot_stride, int32_t num_pages,
+                                   int32_t page_size, const uint32_t* page_table,
+                                   int32_t max_pages_per_seq, uint32_t layer_idx,
+                                   const uint32_t* buffer_row_offsets,
+                                   const uint32_t* cache_offsets, int32_t batch,
+                                   int32_t buffer_length, int32_t kv_lora_rank,
+                                   int32_t rope_dim, const uint8_t* w_e4m3,
+                                   const float* w_scale, int32_t n_out, uint16_t* k_latent,
+                                   uint16_t* k_buffer, uint8_t* q_latent, float* q_scale,
+                                   uint8_t* row_written) {
+    int status = 0;
+    const int32_t C = kv_lora_rank + rope_dim;
+    const int32_t kblocks = kv_lora_rank / 128;
+    const uint8_t* layer = cache + (int64_t)layer_idx * layer_stride;
+    for (int32_t b = 0; b < batch; ++b) {
+        uint32_t begin = buffer_row_offsets[b];
+        uint32_t end = buffer_row_offsets[b + 1];
+        for (uint32_t i = 0; begin + i < end; ++i) {
+            uint64_t r = (uint64_t)begin + i;
+            if (r >= (uint64_t)buffer_length) break;
+            uint64_t t = (uint64_t)cache_offsets[b] + i;
+            int64_t off = token_offset(page_table, max_pages_per_seq, num_pages, page_size,
+                                       page_stride, slot_stride, b, t);
+            if (off < 0) {
+                status = 4;
+                continue;
+            }
+            qslot_load(layer + off, kv_lora_rank, rope_dim, k_latent + r * (uint64_t)C,
+                       q_latent + r * (uint64_t)kv_lora_rank, q_scale + r * (uint64_t)kblocks);
+            fp8_row_product(q_latent + r * (uint64_t)kv_lora_rank, q_scale + r * (uint64_t)kblocks,
+                            w_e4m3, w_scale, kv_lora_rank, n_out, k_buffer + r * (uint64_t)n_out);
+            if (row_written) row_written[r] = 1;
+        }
+    }
+    return status;
+}
+
+/* Single-row form of oracle_decompress_k_qcache_fp8 (returns 1 if no request covers r). */
+int oracle_decompress_k_qcache_fp8_row(const uint8_t* cache, int64_t layer_stride,
+                                       int64_t page_stride, int64_t slot_stride,
+                                       int32_t num_pages, int32_t page_size,
+                                       const uint32_t* page_table, int32_t max_pages_per_seq,
+                                       uint32_t layer_idx, const uint32_t* buffer_row_offsets,
+                                       const uint32_t* cache_offsets, int32_t batch,
+                                       int32_t buffer_length, int32_t kv_lora_rank,
+                                       int32_t rope_dim, const uint8_t* w_e4m3,
+                                       const float* w_scale, int32_t n_out, int64_t r,
+                                       uint16_t* latent_row, uint16_t* k_row, uint8_t* q_row,
+                                       float* scale_row) {
+    if (r < 0 || r >= buffer_length) return 1;
+    for (int32_t b = 0; b < batch; ++b) {
+        if ((uint64_t)buffer_row_offsets[b] <= (uint64_t)r &&
+            (uint64_t)r < (uint64_t)buffer_row_offsets[b + 1]) {
+            uint64_t t = (uint64_t)cache_offsets[b] + ((uint64_t)r - buffer_row_offsets[b]);
+            int64_t off = token_offset(page_table, max_pages_per_seq, num_pages, page_size,
+                                       page_stride, slot_stride, b, t);
+            if (off < 0) return 4;
+            qslot_load(cache + (int64_t)layer_idx * layer_stride + off, kv_lora_rank, rope_dim,
+                       latent_row, q_row, scale_row);
+            fp8_row_product(q_row, scale_row, w_e4m3, w_scale, kv_lora_rank, n_out, k_row);
+            return 0;
+        }
+    }
+    return 1;
 }
 
 /* ------------------------------------------------------------------------------------ */

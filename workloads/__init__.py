@@ -73,6 +73,33 @@ def quantize_weight_e4m3(w: torch.Tensor, block: int = 128):
     return q.view(torch.uint8).numpy().copy(), scale.to(torch.float32).numpy().copy()
 
 
+SENTINEL_QBYTE = 0xA5   # unused bytes of a quantised slot, and untouched quantised slots
+
+
+def qslot_payload_bytes(kv_lora_rank: int, rope_dim: int) -> int:
+    """Bytes a quantised slot holds: R e4m3 codes, P bf16 rope values, R/128 fp32 scales."""
+    return kv_lora_rank + 2 * rope_dim + 4 * (kv_lora_rank // 128)
+
+
+def quantized_latent_slots(shape, kv_lora_rank, rope_dim, slot_bytes, g):
+    """Input preparation for a quantised latent cache of `shape` (layers, pages, page_size)
+    slots: nope values ~N(0, 1) drawn in fp32, per 128-column block scale = amax / 448 and
+    codes = torch's float8_e4m3fn cast of x / scale (as the FP8 weights are prepared), rope
+    ~N(0, 1) bf16; bytes past the payload hold SENTINEL_QBYTE."""
+    R, P = kv_lora_rank, rope_dim
+    x = torch.randn(*shape, R // 128, 128, generator=g, dtype=torch.float32)
+    amax = x.abs().amax(dim=-1)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    codes = (x / scale[..., None]).reshape(*shape, R).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    rope = bf16_normal((*shape, P), 1.0, g)
+    out = np.full((*shape, slot_bytes), SENTINEL_QBYTE, np.uint8)
+    out[..., :R] = codes
+    out[..., R:R + 2 * P] = rope.view(np.uint8).reshape(*shape, 2 * P)
+    out[..., R + 2 * P:R + 2 * P + 4 * (R // 128)] = (
+        scale.to(torch.float32).numpy().view(np.uint8).reshape(*shape, 4 * (R // 128)))
+    return out
+
+
 @dataclass
 class DecompressInputs:
     """One decompress problem.  cache is [num_layers, num_pages, page_size, slot_elems]."""
@@ -94,6 +121,11 @@ class DecompressInputs:
     w_uv_scale: Optional[np.ndarray] = None  # float32 [num_heads*v_head_dim/128, kv_lora_rank/128]
     lengths: Optional[np.ndarray] = None
     meta: dict = field(default_factory=dict)
+
+    @property
+    def quantised(self) -> bool:
+        """cache holds quantised slots (uint8 bytes; strides then count bytes)."""
+        return self.cache.dtype == np.uint8
 
     @property
     def batch(self) -> int:
@@ -121,7 +153,8 @@ class DecompressInputs:
 
     @property
     def strides(self):
-        """(layer_stride, page_stride, slot_stride) in elements."""
+        """(layer_stride, page_stride, slot_stride) in elements of `cache` (bytes for a
+        quantised cache)."""
         _, P, S, E = self.cache.shape
         return P * S * E, S * E, E
 
@@ -192,6 +225,22 @@ def make_decompress(name, seed, lengths, cache_offsets, page_size, kv_lora_rank,
     return d
 
 
+def make_qcache_decompress(name, seed, lengths, cache_offsets, page_size, kv_lora_rank, rope_dim,
+                           n_out, num_layers=1, layer_idx=0, extra_pages=0, slot_pad=0,
+                           page_table=None, num_pages=None, buffer_length=None) -> DecompressInputs:
+    """The FP8 decompress problem of make_decompress (same rows, pages and e4m3 weight) over
+    a quantised latent cache: slots of qslot_payload_bytes rounded up to 16 (+ slot_pad)
+    bytes from quantized_latent_slots, drawn from their own generator (seed + 7919)."""
+    d = make_decompress(name, seed, lengths, cache_offsets, page_size, kv_lora_rank, rope_dim,
+                        n_out, num_layers=num_layers, layer_idx=layer_idx,
+                        extra_pages=extra_pages, fp8=True, page_table=page_table,
+                        num_pages=num_pages, buffer_length=buffer_length)
+    slot_bytes = (qslot_payload_bytes(kv_lora_rank, rope_dim) + 15) // 16 * 16 + slot_pad
+    d.cache = quantized_latent_slots(d.cache.shape[:3], kv_lora_rank, rope_dim, slot_bytes,
+                                     _gen(seed + 7919))
+    return d
+
+
 def add_v_weight(d: DecompressInputs, num_heads, v_head_dim, seed, w_std=None, fp8=False,
                  int_values=False) -> DecompressInputs:
     """Adds a w_uv [num_heads, v_head_dim, kv_lora_rank] drawn from its own seeded generator
@@ -244,6 +293,14 @@ def deepseek_decompress(seed=1001, fp8=False) -> DecompressInputs:
                            seed + 1, lengths, co, 128, 512, 64, 16384, fp8=fp8)
 
 
+def deepseek_qcache_decompress(seed=1001) -> DecompressInputs:
+    """The DeepSeek-V3 FP8 decompress (same 16 requests, rows, pages and W_k) over a
+    quantised latent cache (656-byte slots: 512 e4m3 codes, 64 bf16 rope, 4 fp32 scales)."""
+    lengths, co = deepseek_lengths(seed)
+    return make_qcache_decompress("deepseek_v3_fp8_qcache_decompress", seed + 1, lengths, co, 128,
+                                  512, 64, 16384)
+
+
 def long_context_decompress(seed=1003) -> DecompressInputs:
     """4 requests x 32768 cached tokens (buffer_length 131072), 1024 shuffled pages."""
     return make_decompress("long_context_decompress", seed, [32768] * 4, [0] * 4, 128, 512, 64,
@@ -260,7 +317,8 @@ class CacheWriteInputs:
     input_row_offsets: np.ndarray  # uint32 [batch + 1]
     cache_lengths: np.ndarray      # uint32 [batch]
     page_table: np.ndarray         # uint32 [batch, max_pages_per_seq]
-    cache: np.ndarray              # uint16 bf16, pre-filled with SENTINEL_CACHE
+    cache: np.ndarray              # uint16 bf16 pre-filled with SENTINEL_CACHE, or (quantised
+                                   # cache) uint8 slots pre-filled with SENTINEL_QBYTE
     gamma: np.ndarray              # float32 [R]
     epsilon: float
     freqs_cis: np.ndarray          # float32 [max_seq_len, P]: P/2 (cos, sin) pairs per position
@@ -294,16 +352,22 @@ class CacheWriteInputs:
         return Pg * S * E, S * E, E
 
     @property
+    def quantised(self) -> bool:
+        return self.cache.dtype == np.uint8
+
+    @property
     def bytes_moved(self) -> int:
-        """Algorithmic HBM bytes: read every new row and write it into the cache (bf16), read
-        gamma and the freqs_cis table once."""
+        """Algorithmic HBM bytes: read every new row and write it into the cache (a bf16 row,
+        or a quantised slot's payload), read gamma and the freqs_cis table once."""
         rows = int(self.input_row_offsets[-1])
-        return 2 * rows * self.row_elems * 2 + self.gamma.nbytes + self.freqs_cis.nbytes
+        out = (qslot_payload_bytes(self.kv_lora_rank, self.rope_dim) if self.quantised
+               else 2 * self.row_elems)
+        return rows * (2 * self.row_elems + out) + self.gamma.nbytes + self.freqs_cis.nbytes
 
 
 def make_cache_write(name, seed, new_tokens, cache_lengths, kv_lora_rank, rope_dim, page_size,
                      num_layers=1, layer_idx=0, extra_pages=0, epsilon=1e-6, max_seq_len=None,
-                     latent_std=1.0) -> CacheWriteInputs:
+                     latent_std=1.0, quantised=False, slot_pad=0) -> CacheWriteInputs:
     """Seeded cache-write problem: latent ~N(0, latent_std^2) bf16, gamma ~1 + N(0, 0.1^2)
     fp32, freqs_cis = (cos phi, sin phi) for phi ~U[0, 2 pi) drawn per position and pair
     (any unit complex numbers are valid RoPE factors), pages assigned in one seeded
@@ -325,7 +389,11 @@ def make_cache_write(name, seed, new_tokens, cache_lengths, kv_lora_rank, rope_d
         max_seq_len = int((cl + new_tokens).max()) + 1
     phi = torch.rand(max_seq_len, rope_dim // 2, generator=g, dtype=torch.float64) * (2 * math.pi)
     freqs = torch.stack([torch.cos(phi), torch.sin(phi)], dim=-1).reshape(max_seq_len, rope_dim)
-    cache = np.full((num_layers, total_pages, page_size, C), SENTINEL_CACHE, np.uint16)
+    if quantised:
+        slot_bytes = (qslot_payload_bytes(kv_lora_rank, rope_dim) + 15) // 16 * 16 + slot_pad
+        cache = np.full((num_layers, total_pages, page_size, slot_bytes), SENTINEL_QBYTE, np.uint8)
+    else:
+        cache = np.full((num_layers, total_pages, page_size, C + slot_pad), SENTINEL_CACHE, np.uint16)
     return CacheWriteInputs(name=name, latent=latent, input_row_offsets=iro,
                             cache_lengths=cl.astype(np.uint32), page_table=pt, cache=cache,
                             gamma=gamma.numpy().copy(), epsilon=float(epsilon),
@@ -333,15 +401,15 @@ def make_cache_write(name, seed, new_tokens, cache_lengths, kv_lora_rank, rope_d
                             kv_lora_rank=kv_lora_rank, rope_dim=rope_dim, layer_idx=layer_idx)
 
 
-def cache_write_path(seed=1007) -> CacheWriteInputs:
+def cache_write_path(seed=1007, quantised=False) -> CacheWriteInputs:
     """DeepSeek-V3 latent cache write of a prefill batch: 32 requests, new ~U[1024, 4096]
     tokens after cache_len ~U[0, 2048], latent 512 + 64, page_size 128, 2 layers (layer 1
-    written)."""
+    written); bf16 slots, or quantised 656-byte slots."""
     g = _gen(seed)
     new = torch.randint(1024, 4097, (32,), generator=g).numpy()
     cl = torch.randint(0, 2049, (32,), generator=g).numpy()
-    return make_cache_write("cache_write_path", seed + 1, new, cl, 512, 64, 128, num_layers=2,
-                            layer_idx=1)
+    return make_cache_write("cache_write_q_path" if quantised else "cache_write_path", seed + 1,
+                            new, cl, 512, 64, 128, num_layers=2, layer_idx=1, quantised=quantised)
 
 
 @dataclass
@@ -449,4 +517,6 @@ WORKLOADS = {
     "deepseek_v3_fp8_decompress_kv": lambda: deepseek_decompress_kv(1001, fp8=True),
     "kv_matmul_write_path": kv_matmul_write_path,
     "cache_write_path": cache_write_path,
+    "cache_write_q_path": lambda: cache_write_path(1007, quantised=True),
+    "deepseek_v3_fp8_qcache_decompress": deepseek_qcache_decompress,
 }
