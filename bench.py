@@ -51,6 +51,7 @@ KERNEL_SOURCES = {
     "fp8_gather_quantize_kernel": ["decompress_fp8.cu"],
     "kv_matmul_kernel": ["kv_matmul.cu"],
     "cache_write_kernel": ["cache_write.cu"],
+    "fp8_gather_qcache_kernel": ["decompress_fp8.cu"],
 }
 
 
@@ -184,6 +185,17 @@ def fp8_algorithmic_bytes(d) -> int:
     n = d.n_out + d.n_out_v
     R = d.kv_lora_rank
     return rows * (4 * d.latent_cols + 2 * n + R + 4 * (R // 128)) + n * R
+
+
+def qcache_algorithmic_bytes(d) -> int:
+    """FP8 decompress from a quantised cache, per covered row: the slot payload read
+    (R + 2P + 4R/128 bytes), the dequantised bf16 latent row written (2C), the codes and
+    scales written to the workspace (R + 4R/128), one bf16 output row (2N); the e4m3
+    weight once."""
+    rows = min(int(d.buffer_row_offsets[-1]), d.buffer_length)
+    R, P = d.kv_lora_rank, d.rope_dim
+    payload = R + 2 * P + 4 * (R // 128)
+    return rows * (payload + 2 * d.latent_cols + R + 4 * (R // 128) + 2 * d.n_out) + d.n_out * R
 
 
 def _device_problem(d, fp8=False):
@@ -326,16 +338,30 @@ def run_ours(args, rank, world, local_rank):
         "roofline_frac": t_roof / tk}
     del gk
     from gpu_util import DeviceCacheWrite
-    cw = workloads.WORKLOADS["cache_write_path"]()
-    gc = DeviceCacheWrite(cw)
-    tc = _time_steps(gc.run, sec_steps, 3, flush, stream) / sec_steps
-    assert int(gc.status.item()) == 0
-    extra["cache_write"] = {
-        "workload": cw.name, "rows": cw.total_rows, "ms": tc * 1e3,
-        "rows_per_s": cw.total_rows / tc, "gbs": cw.bytes_moved / tc / 1e9,
-        "hbm_frac_of_measured": cw.bytes_moved / tc / 1e9 / peaks["hbm_gbs"],
-        "traffic": profiled_traffic("cache_write_kernel"), "launches_per_step": 1}
-    del gc
+    for key, wl in [("cache_write", "cache_write_path"), ("cache_write_q", "cache_write_q_path")]:
+        cw = workloads.WORKLOADS[wl]()
+        gc = DeviceCacheWrite(cw)
+        tc = _time_steps(gc.run, sec_steps, 3, flush, stream) / sec_steps
+        assert int(gc.status.item()) == 0
+        extra[key] = {
+            "workload": cw.name, "rows": cw.total_rows, "ms": tc * 1e3,
+            "rows_per_s": cw.total_rows / tc, "gbs": cw.bytes_moved / tc / 1e9,
+            "hbm_frac_of_measured": cw.bytes_moved / tc / 1e9 / peaks["hbm_gbs"],
+            "traffic": profiled_traffic("cache_write_kernel") if key == "cache_write" else None,
+            "launches_per_step": 1}
+        del gc, cw
+    # FP8 decompress from a quantised cache (codes and scales gathered as they are)
+    dq = workloads.WORKLOADS["deepseek_v3_fp8_qcache_decompress"]()
+    gq = _device_problem(dq, fp8=True)
+    tq = _time_steps(gq.run, sec_steps, 3, flush, stream) / sec_steps
+    assert int(gq.status.item()) == 0
+    bq = qcache_algorithmic_bytes(dq)
+    extra["fp8_qcache_decompress"] = {
+        "workload": dq.name, "rows": dq.buffer_length, "ms": tq * 1e3,
+        "tflops": dq.flops / tq / 1e12, "rows_per_s": dq.buffer_length / tq,
+        "hbm_gbs": bq / tq / 1e9, "hbm_frac_of_measured": bq / tq / 1e9 / peaks["hbm_gbs"],
+        "launches_per_step": 2}
+    del gq, dq
 
     # ---------------- end to end: host buffers through the C ABI ----------------
     e2e = run_e2e(d, max(3, min(args.steps, 10)))

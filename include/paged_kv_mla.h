@@ -97,6 +97,40 @@ typedef struct {
 } pkm_paged_cache;
 
 /*
+ * A quantised paged latent cache (PagedKVCacheCollection's type parameters scale_dtype_ and
+ * quantization_granularity_; the pages give no layout).  One token's slot is a byte string:
+ *     bytes [0, R)                     e4m3 codes of the R = kv_lora_rank nope columns
+ *     bytes [R, R + 2P)                the P = rope_dim rope columns, bf16
+ *     bytes [R + 2P, R + 2P + 4R/128)  fp32 scales, one per 128 columns (scale_dtype_ =
+ *                                      float32, quantization_granularity_ = 128)
+ * A nope value is fl32(e4m3(code) * scale).  The codes and scales are those the FP8
+ * decompress's quantisation (s = amax/448 per 128-column block, q = e4m3_rne(x / s)) makes
+ * of the bf16 row a bf16 cache would hold, so the quantised cache (656 bytes a token for
+ * DeepSeek-V3 against 1152) feeds the FP8 product the same operands.
+ *
+ *   data             device bytes, 16-byte aligned.
+ *   layer_stride, page_stride, slot_stride   bytes, multiples of 16; slot_stride >= the
+ *                    payload R + 2P + 4R/128.
+ *   kv_lora_rank     R: a multiple of 128, 128..512 (1024 for the cache write).
+ *   rope_dim         P: a multiple of 8, at most 256.
+ *   cache_lengths    [batch] existing lengths (the cache write only).
+ */
+typedef struct {
+    void* data;
+    int64_t layer_stride;
+    int64_t page_stride;
+    int64_t slot_stride;
+    int32_t num_layers;
+    int32_t num_pages;
+    int32_t page_size;
+    int32_t kv_lora_rank;
+    int32_t rope_dim;
+    const uint32_t* page_table;
+    int32_t max_pages_per_seq;
+    const uint32_t* cache_lengths;
+} pkm_quant_cache;
+
+/*
  * bf16 latent-K decompress.
  * Source: generic_flare_mla_decompress_k_cache_ragged_paged -- signature, description
  * ("gathers ... into k_latent_buffer using buffer_row_offsets and cache_offsets, then
@@ -274,6 +308,51 @@ pkm_status mla_cache_write_paged(const void* latent, const uint32_t* input_row_o
                                  const float* freqs_cis, int32_t max_seq_len,
                                  const pkm_paged_cache* cache, uint32_t layer_idx,
                                  int32_t* dev_status, void* stream);
+
+/*
+ * FP8 latent-K decompress from a quantised paged cache.
+ * Source: generic_flare_mla_decompress_k_cache_ragged_paged (rows, tokens, page walk) with
+ * the FP8 product of mla_prefill_decode_graph_fp8 (Args w_k, w_k_scale) over a
+ * PagedKVCacheCollection with scale_dtype_ / quantization_granularity_ (layout above).
+ *
+ * The rows and cache tokens of mla_decompress_k_paged.  Every written row r takes its
+ * slot's codes and scales as they are (workspace: codes [L, R] at 0, scales [L, R/128] at
+ * align256(L*R), the layout of mla_decompress_k_paged_fp8), and
+ *     k_latent_buffer[r, k]     = bf16_rne(fl32(e4m3(code_k) * scale_{k/128})),  k < R
+ *     k_latent_buffer[r, R + j] = the slot's rope value j, bit for bit
+ *     k_buffer[r, n] = bf16( sum_kb scale[kb] * w_k_scale[n/128, kb]
+ *                              * sum_{k in kb} code_k * w_k_e4m3[n, k] )
+ * (no quantisation step: the cache already holds the operands).
+ *
+ *   cache             host struct (kv_lora_rank 128..512, a multiple of 128).
+ *   k_latent_buffer   device bf16 [buffer_length, R + P], 16-byte aligned, or null to skip.
+ *   workspace         >= mla_decompress_k_paged_fp8_workspace_size(buffer_length, R) bytes,
+ *                     256-byte aligned.
+ *   other arguments   as for mla_decompress_k_paged_fp8.
+ */
+pkm_status mla_decompress_k_paged_fp8_qcache(const pkm_quant_cache* cache, uint32_t layer_idx,
+                                             const uint32_t* buffer_row_offsets,
+                                             const uint32_t* cache_offsets, int32_t batch,
+                                             int32_t buffer_length, const void* w_k_e4m3,
+                                             const float* w_k_scale, int32_t n_out,
+                                             void* k_latent_buffer, void* k_buffer,
+                                             void* workspace, size_t workspace_bytes,
+                                             int32_t* dev_status, void* stream);
+
+/*
+ * Cache write into a quantised paged cache: the rows mla_cache_write_paged would store
+ * (RMSNorm with kv_norm_gamma, RoPE with freqs_cis, rounded to bf16), quantised per
+ * 128-column block into the slot layout above (s = amax/448 in fp32, 1 for an all-zero
+ * block; q = e4m3_rne_satfinite(y / s) with the division in fp32).  Only the slot's payload
+ * bytes are written.  Arguments as for mla_cache_write_paged, with R and P taken from the
+ * descriptor (R a multiple of 128, at most 1024).
+ */
+pkm_status mla_cache_write_paged_qcache(const void* latent, const uint32_t* input_row_offsets,
+                                        int32_t batch, int32_t total_rows,
+                                        const float* kv_norm_gamma, float epsilon,
+                                        const float* freqs_cis, int32_t max_seq_len,
+                                        const pkm_quant_cache* cache, uint32_t layer_idx,
+                                        int32_t* dev_status, void* stream);
 
 /*
  * FP8 decompress for callers that cannot allocate device memory.  The paper has no

@@ -52,6 +52,15 @@ class _CCache(ctypes.Structure):
                 ("max_pages_per_seq", ctypes.c_int32), ("cache_lengths", ctypes.c_void_p)]
 
 
+class _CQuantCache(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("layer_stride", ctypes.c_int64),
+                ("page_stride", ctypes.c_int64), ("slot_stride", ctypes.c_int64),
+                ("num_layers", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("kv_lora_rank", ctypes.c_int32),
+                ("rope_dim", ctypes.c_int32), ("page_table", ctypes.c_void_p),
+                ("max_pages_per_seq", ctypes.c_int32), ("cache_lengths", ctypes.c_void_p)]
+
+
 _vp, _i32, _u32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_size_t
 _lib.pkm_status_string.argtypes = [ctypes.c_int]
 _lib.pkm_status_string.restype = ctypes.c_char_p
@@ -64,6 +73,13 @@ _lib.mla_decompress_k_paged_fp8.argtypes = [ctypes.POINTER(_CCache), _u32, _vp, 
                                             _i32, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp,
                                             _vp]
 _lib.mla_decompress_k_paged_fp8.restype = ctypes.c_int
+_lib.mla_decompress_k_paged_fp8_qcache.argtypes = [ctypes.POINTER(_CQuantCache), _u32, _vp, _vp,
+                                                   _i32, _i32, _vp, _vp, _i32, _vp, _vp, _vp,
+                                                   _sz, _vp, _vp]
+_lib.mla_decompress_k_paged_fp8_qcache.restype = ctypes.c_int
+_lib.mla_cache_write_paged_qcache.argtypes = [_vp, _vp, _i32, _i32, _vp, ctypes.c_float, _vp,
+                                              _i32, ctypes.POINTER(_CQuantCache), _u32, _vp, _vp]
+_lib.mla_cache_write_paged_qcache.restype = ctypes.c_int
 _lib.mla_decompress_kv_paged.argtypes = [ctypes.POINTER(_CCache), _u32, _vp, _vp, _i32, _i32, _i32,
                                          _i32, _vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
 _lib.mla_decompress_kv_paged.restype = ctypes.c_int
@@ -134,6 +150,33 @@ class PagedCache:
                        _ptr(self.cache_lengths))
 
 
+@dataclass
+class QuantCache:
+    """A quantised paged latent cache described by byte strides; see pkm_quant_cache.
+
+    data: storage of the slots (any dtype and shape; only its base pointer is used).  A slot
+    holds kv_lora_rank e4m3 codes, rope_dim bf16 values and kv_lora_rank/128 fp32 scales.
+    """
+    data: torch.Tensor
+    page_table: torch.Tensor
+    layer_stride: int
+    page_stride: int
+    slot_stride: int
+    num_layers: int
+    num_pages: int
+    page_size: int
+    kv_lora_rank: int
+    rope_dim: int
+    cache_lengths: Optional[torch.Tensor] = None
+
+    def c_struct(self) -> _CQuantCache:
+        return _CQuantCache(self.data.data_ptr(), int(self.layer_stride), int(self.page_stride),
+                            int(self.slot_stride), int(self.num_layers), int(self.num_pages),
+                            int(self.page_size), int(self.kv_lora_rank), int(self.rope_dim),
+                            self.page_table.data_ptr(), int(self.page_table.shape[-1]),
+                            _ptr(self.cache_lengths))
+
+
 def _check(code: int, where: str, check: bool) -> int:
     if check and code != PKM_OK:
         raise PkmError(code, where)
@@ -201,6 +244,41 @@ def mla_decompress_k_paged_fp8(cache: PagedCache, layer_idx: int,
         int(w_k_e4m3.shape[0]), _ptr(k_latent_buffer), _ptr(k_buffer), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
     return _check(code, "mla_decompress_k_paged_fp8", check)
+
+
+def mla_decompress_k_paged_fp8_qcache(cache: QuantCache, layer_idx: int,
+                                      buffer_row_offsets: torch.Tensor, cache_offsets: torch.Tensor,
+                                      buffer_length: int, w_k_e4m3: torch.Tensor,
+                                      w_k_scale: torch.Tensor, k_latent_buffer: Optional[torch.Tensor],
+                                      k_buffer: torch.Tensor, workspace: torch.Tensor,
+                                      dev_status: Optional[torch.Tensor] = None, stream=None,
+                                      check: bool = True) -> int:
+    """FP8 decompress reading codes and scales straight from a quantised cache;
+    k_latent_buffer (dequantised bf16 rows) may be None."""
+    c = cache.c_struct()
+    batch = int(buffer_row_offsets.shape[0]) - 1
+    code = _lib.mla_decompress_k_paged_fp8_qcache(
+        ctypes.byref(c), int(layer_idx), _ptr(buffer_row_offsets), _ptr(cache_offsets), batch,
+        int(buffer_length), _ptr(w_k_e4m3), _ptr(w_k_scale), int(w_k_e4m3.shape[0]),
+        _ptr(k_latent_buffer), _ptr(k_buffer), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
+    return _check(code, "mla_decompress_k_paged_fp8_qcache", check)
+
+
+def mla_cache_write_paged_qcache(latent: torch.Tensor, input_row_offsets: torch.Tensor,
+                                 kv_norm_gamma: torch.Tensor, epsilon: float,
+                                 freqs_cis: torch.Tensor, cache: QuantCache, layer_idx: int,
+                                 dev_status: Optional[torch.Tensor] = None, stream=None,
+                                 check: bool = True) -> int:
+    """RMSNorm + RoPE of new latent rows, quantised into a quantised cache's slots."""
+    c = cache.c_struct()
+    batch = int(input_row_offsets.shape[0]) - 1
+    code = _lib.mla_cache_write_paged_qcache(_ptr(latent), _ptr(input_row_offsets), batch,
+                                             int(latent.shape[0]), _ptr(kv_norm_gamma),
+                                             float(epsilon), _ptr(freqs_cis),
+                                             int(freqs_cis.shape[0]), ctypes.byref(c),
+                                             int(layer_idx), _ptr(dev_status), _stream(stream))
+    return _check(code, "mla_cache_write_paged_qcache", check)
 
 
 def mla_decompress_kv_paged_fp8(cache: PagedCache, layer_idx: int,

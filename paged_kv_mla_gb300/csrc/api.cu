@@ -294,20 +294,48 @@ pkm_status decompress_bf16(const pkm_paged_cache* cache, uint32_t layer_idx,
 
 // Body of the FP8 entry points: K alone (v.w_uv == nullptr) or K and V, the activations
 // quantised once for both.
+// Checks of a quantised cache for the decompress (the bf16 cache's check_decompress).
+pkm_status check_qdecompress(const pkm_quant_cache* cache, uint32_t layer_idx, const uint32_t* bro,
+                             const uint32_t* co, const void* w, void* k_latent, void* k_buffer) {
+    if (cache == nullptr || bro == nullptr || co == nullptr || w == nullptr ||
+        k_buffer == nullptr || cache->data == nullptr || cache->page_table == nullptr)
+        return PKM_ERR_INVALID_ARG;
+    if (cache->num_layers <= 0 || layer_idx >= static_cast<uint32_t>(cache->num_layers) ||
+        cache->num_pages <= 0 || cache->page_size <= 0 || cache->max_pages_per_seq <= 0)
+        return PKM_ERR_INVALID_ARG;
+    const int64_t payload = static_cast<int64_t>(cache->kv_lora_rank) + 2 * cache->rope_dim +
+                            4 * (cache->kv_lora_rank / 128);
+    if (cache->layer_stride < 0 || cache->layer_stride % 16 != 0 || cache->page_stride < 0 ||
+        cache->page_stride % 16 != 0 || cache->slot_stride % 16 != 0 ||
+        cache->slot_stride < payload)
+        return PKM_ERR_INVALID_ARG;
+    if (!aligned16(cache->data) || !aligned16(w) || !aligned16(k_buffer) ||
+        (k_latent != nullptr && !aligned16(k_latent)))
+        return PKM_ERR_INVALID_ARG;
+    return PKM_OK;
+}
+
 pkm_status decompress_fp8(const pkm_paged_cache* cache, uint32_t layer_idx,
                           const uint32_t* buffer_row_offsets, const uint32_t* cache_offsets,
                           int32_t batch, int32_t buffer_length, int32_t kv_lora_rank,
                           int32_t rope_dim, const void* w_k_e4m3, const float* w_k_scale,
                           int32_t n_out, const VOperands& v, void* k_latent_buffer,
                           void* k_buffer, void* workspace, size_t workspace_bytes,
-                          int32_t* dev_status, void* stream) {
+                          int32_t* dev_status, void* stream,
+                          const pkm_quant_cache* qcache = nullptr) {
     bool empty = false;
     pkm_status st = check_decompress_sizes(batch, buffer_length, kv_lora_rank, rope_dim, n_out,
                                            &empty);
     if (st != PKM_OK || empty) return st;
-    st = check_decompress(cache, layer_idx, buffer_row_offsets, cache_offsets, batch,
-                                     buffer_length, kv_lora_rank, rope_dim, w_k_e4m3, n_out,
-                                     k_latent_buffer, k_buffer);
+    if (qcache != nullptr) {
+        if (rope_dim % 8 != 0 || rope_dim > 256) return PKM_ERR_UNSUPPORTED;
+        st = check_qdecompress(qcache, layer_idx, buffer_row_offsets, cache_offsets, w_k_e4m3,
+                               k_latent_buffer, k_buffer);
+    } else {
+        st = check_decompress(cache, layer_idx, buffer_row_offsets, cache_offsets, batch,
+                              buffer_length, kv_lora_rank, rope_dim, w_k_e4m3, n_out,
+                              k_latent_buffer, k_buffer);
+    }
     if (st != PKM_OK) return st;
     if (w_k_scale == nullptr || workspace == nullptr) return PKM_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKM_ERR_INVALID_ARG;
@@ -316,9 +344,28 @@ pkm_status decompress_fp8(const pkm_paged_cache* cache, uint32_t layer_idx,
     if (workspace_bytes < mla_decompress_k_paged_fp8_workspace_size(buffer_length, kv_lora_rank))
         return PKM_ERR_INVALID_ARG;
     const int32_t nv = v.w_uv != nullptr ? v.n_v : 0;
-    DecompressArgs a = make_decompress_args(cache, layer_idx, buffer_row_offsets, cache_offsets,
-                                            batch, buffer_length, kv_lora_rank, rope_dim, n_out,
-                                            k_latent_buffer, k_buffer, dev_status, 128);
+    DecompressArgs a{};
+    if (qcache != nullptr) {
+        // the same problem over byte strides: the page walk is unit-agnostic
+        pkm_paged_cache view{};
+        view.data = qcache->data;
+        view.page_stride = qcache->page_stride;
+        view.slot_stride = qcache->slot_stride;
+        view.num_pages = qcache->num_pages;
+        view.page_size = qcache->page_size;
+        view.page_table = qcache->page_table;
+        view.max_pages_per_seq = qcache->max_pages_per_seq;
+        a = make_decompress_args(&view, 0, buffer_row_offsets, cache_offsets, batch,
+                                 buffer_length, kv_lora_rank, rope_dim, n_out, k_latent_buffer,
+                                 k_buffer, dev_status, 128);
+        a.cache_layer = nullptr;
+        a.qcache_layer = static_cast<const uint8_t*>(qcache->data) +
+                         static_cast<int64_t>(layer_idx) * qcache->layer_stride;
+    } else {
+        a = make_decompress_args(cache, layer_idx, buffer_row_offsets, cache_offsets, batch,
+                                 buffer_length, kv_lora_rank, rope_dim, n_out, k_latent_buffer,
+                                 k_buffer, dev_status, 128);
+    }
     a.n_tiles_k = a.n_tiles;
     if (nv > 0) {
         a.v_buffer = static_cast<uint16_t*>(v.v_buffer);
@@ -352,7 +399,9 @@ pkm_status decompress_fp8(const pkm_paged_cache* cache, uint32_t layer_idx,
         tm_wv = tm_w;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (pkm::launch_fp8_gather_quantize(a, x, sms, s) != cudaSuccess) return PKM_ERR_CUDA;
+    const cudaError_t ge = qcache != nullptr ? pkm::launch_fp8_gather_qcache(a, x, sms, s)
+                                             : pkm::launch_fp8_gather_quantize(a, x, sms, s);
+    if (ge != cudaSuccess) return PKM_ERR_CUDA;
     return pkm::launch_decompress_fp8_gemm(tm_q, tm_w, tm_wv, a, x, sms, s) == cudaSuccess
                ? PKM_OK
                : PKM_ERR_CUDA;
@@ -441,31 +490,88 @@ pkm_status mla_decompress_kv_paged_fp8(const pkm_paged_cache* cache, uint32_t la
                           stream);
 }
 
-pkm_status mla_cache_write_paged(const void* latent, const uint32_t* input_row_offsets,
-                                 int32_t batch, int32_t total_rows, int32_t kv_lora_rank,
-                                 int32_t rope_dim, const float* kv_norm_gamma, float epsilon,
-                                 const float* freqs_cis, int32_t max_seq_len,
-                                 const pkm_paged_cache* cache, uint32_t layer_idx,
-                                 int32_t* dev_status, void* stream) {
+pkm_status mla_decompress_k_paged_fp8_qcache(const pkm_quant_cache* cache, uint32_t layer_idx,
+                                             const uint32_t* buffer_row_offsets,
+                                             const uint32_t* cache_offsets, int32_t batch,
+                                             int32_t buffer_length, const void* w_k_e4m3,
+                                             const float* w_k_scale, int32_t n_out,
+                                             void* k_latent_buffer, void* k_buffer,
+                                             void* workspace, size_t workspace_bytes,
+                                             int32_t* dev_status, void* stream) {
+    if (cache == nullptr) return PKM_ERR_INVALID_ARG;
+    return decompress_fp8(nullptr, layer_idx, buffer_row_offsets, cache_offsets, batch,
+                          buffer_length, cache->kv_lora_rank, cache->rope_dim, w_k_e4m3,
+                          w_k_scale, n_out, VOperands{}, k_latent_buffer, k_buffer, workspace,
+                          workspace_bytes, dev_status, stream, cache);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Body of both cache-write entry points: a bf16 cache, or (qcache) a quantised one.
+pkm_status cache_write(const void* latent, const uint32_t* input_row_offsets, int32_t batch,
+                       int32_t total_rows, int32_t kv_lora_rank, int32_t rope_dim,
+                       const float* kv_norm_gamma, float epsilon, const float* freqs_cis,
+                       int32_t max_seq_len, const pkm_paged_cache* cache,
+                       const pkm_quant_cache* qcache, uint32_t layer_idx, int32_t* dev_status,
+                       void* stream) {
     if (batch < 0 || total_rows < 0 || kv_lora_rank <= 0 || rope_dim < 0 || max_seq_len <= 0)
         return PKM_ERR_INVALID_ARG;
     if (batch == 0 || total_rows == 0) return PKM_OK;
     if (latent == nullptr || input_row_offsets == nullptr || kv_norm_gamma == nullptr ||
-        (freqs_cis == nullptr && rope_dim > 0) || cache == nullptr || cache->data == nullptr ||
-        cache->page_table == nullptr || cache->cache_lengths == nullptr)
-        return PKM_ERR_INVALID_ARG;
-    if (cache->num_layers <= 0 || layer_idx >= static_cast<uint32_t>(cache->num_layers) ||
-        cache->num_pages <= 0 || cache->page_size <= 0 || cache->max_pages_per_seq <= 0)
+        (freqs_cis == nullptr && rope_dim > 0))
         return PKM_ERR_INVALID_ARG;
     if (kv_lora_rank % 8 != 0 || kv_lora_rank > 1024 || rope_dim % 8 != 0 || rope_dim > 256)
         return PKM_ERR_UNSUPPORTED;
-    if (cache->row_elems != kv_lora_rank + rope_dim) return PKM_ERR_INVALID_ARG;
-    if (!mult8(cache->layer_stride) || !mult8(cache->page_stride) || !mult8(cache->slot_stride))
-        return PKM_ERR_INVALID_ARG;
-    if (!aligned16(latent) || !aligned16(kv_norm_gamma) || !aligned16(freqs_cis) ||
-        !aligned16(cache->data) || !mult8(cache->layer_stride))
+    if (!aligned16(latent) || !aligned16(kv_norm_gamma) || !aligned16(freqs_cis))
         return PKM_ERR_INVALID_ARG;
     CacheWriteArgs a{};
+    if (qcache != nullptr) {
+        if (qcache->data == nullptr || qcache->page_table == nullptr ||
+            qcache->cache_lengths == nullptr)
+            return PKM_ERR_INVALID_ARG;
+        if (qcache->num_layers <= 0 || layer_idx >= static_cast<uint32_t>(qcache->num_layers) ||
+            qcache->num_pages <= 0 || qcache->page_size <= 0 || qcache->max_pages_per_seq <= 0)
+            return PKM_ERR_INVALID_ARG;
+        if (kv_lora_rank % 128 != 0) return PKM_ERR_UNSUPPORTED;
+        const int64_t payload = static_cast<int64_t>(kv_lora_rank) + 2 * rope_dim +
+                                4 * (kv_lora_rank / 128);
+        if (qcache->layer_stride < 0 || qcache->layer_stride % 16 != 0 ||
+            qcache->page_stride < 0 || qcache->page_stride % 16 != 0 ||
+            qcache->slot_stride % 16 != 0 || qcache->slot_stride < payload ||
+            !aligned16(qcache->data))
+            return PKM_ERR_INVALID_ARG;
+        a.qcache_layer = static_cast<uint8_t*>(qcache->data) +
+                         static_cast<int64_t>(layer_idx) * qcache->layer_stride;
+        a.page_stride = qcache->page_stride;
+        a.slot_stride = qcache->slot_stride;
+        a.num_pages = qcache->num_pages;
+        a.page_size = qcache->page_size;
+        a.max_pages = qcache->max_pages_per_seq;
+        a.page_table = qcache->page_table;
+        a.cache_lengths = qcache->cache_lengths;
+    } else {
+        if (cache == nullptr || cache->data == nullptr || cache->page_table == nullptr ||
+            cache->cache_lengths == nullptr)
+            return PKM_ERR_INVALID_ARG;
+        if (cache->num_layers <= 0 || layer_idx >= static_cast<uint32_t>(cache->num_layers) ||
+            cache->num_pages <= 0 || cache->page_size <= 0 || cache->max_pages_per_seq <= 0)
+            return PKM_ERR_INVALID_ARG;
+        if (cache->row_elems != kv_lora_rank + rope_dim) return PKM_ERR_INVALID_ARG;
+        if (!mult8(cache->layer_stride) || !mult8(cache->page_stride) ||
+            !mult8(cache->slot_stride) || !aligned16(cache->data))
+            return PKM_ERR_INVALID_ARG;
+        a.cache_layer = static_cast<uint16_t*>(cache->data) +
+                        static_cast<int64_t>(layer_idx) * cache->layer_stride;
+        a.page_stride = cache->page_stride;
+        a.slot_stride = cache->slot_stride;
+        a.num_pages = cache->num_pages;
+        a.page_size = cache->page_size;
+        a.max_pages = cache->max_pages_per_seq;
+        a.page_table = cache->page_table;
+        a.cache_lengths = cache->cache_lengths;
+    }
     a.latent = static_cast<const uint16_t*>(latent);
     a.row_offsets = input_row_offsets;
     a.batch = batch;
@@ -476,15 +582,6 @@ pkm_status mla_cache_write_paged(const void* latent, const uint32_t* input_row_o
     a.epsilon = epsilon;
     a.freqs = freqs_cis;
     a.max_seq_len = max_seq_len;
-    a.cache_layer = static_cast<uint16_t*>(cache->data) +
-                    static_cast<int64_t>(layer_idx) * cache->layer_stride;
-    a.page_stride = cache->page_stride;
-    a.slot_stride = cache->slot_stride;
-    a.num_pages = cache->num_pages;
-    a.page_size = cache->page_size;
-    a.max_pages = cache->max_pages_per_seq;
-    a.page_table = cache->page_table;
-    a.cache_lengths = cache->cache_lengths;
     a.status = dev_status;
     a.timeout_ns = wait_timeout_ns();
     int sms = 0;
@@ -492,6 +589,33 @@ pkm_status mla_cache_write_paged(const void* latent, const uint32_t* input_row_o
     return pkm::launch_cache_write(a, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PKM_OK
                : PKM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkm_status mla_cache_write_paged(const void* latent, const uint32_t* input_row_offsets,
+                                 int32_t batch, int32_t total_rows, int32_t kv_lora_rank,
+                                 int32_t rope_dim, const float* kv_norm_gamma, float epsilon,
+                                 const float* freqs_cis, int32_t max_seq_len,
+                                 const pkm_paged_cache* cache, uint32_t layer_idx,
+                                 int32_t* dev_status, void* stream) {
+    return cache_write(latent, input_row_offsets, batch, total_rows, kv_lora_rank, rope_dim,
+                       kv_norm_gamma, epsilon, freqs_cis, max_seq_len, cache, nullptr,
+                       layer_idx, dev_status, stream);
+}
+
+pkm_status mla_cache_write_paged_qcache(const void* latent, const uint32_t* input_row_offsets,
+                                        int32_t batch, int32_t total_rows,
+                                        const float* kv_norm_gamma, float epsilon,
+                                        const float* freqs_cis, int32_t max_seq_len,
+                                        const pkm_quant_cache* cache, uint32_t layer_idx,
+                                        int32_t* dev_status, void* stream) {
+    if (cache == nullptr) return PKM_ERR_INVALID_ARG;
+    return cache_write(latent, input_row_offsets, batch, total_rows, cache->kv_lora_rank,
+                       cache->rope_dim, kv_norm_gamma, epsilon, freqs_cis, max_seq_len, nullptr,
+                       cache, layer_idx, dev_status, stream);
 }
 
 pkm_status kv_matmul_paged(const void* hidden_state, const uint32_t* input_row_offsets,

@@ -23,6 +23,12 @@
 // reduces the sum of squares across the warp and writes the normalised and rotated rows
 // (fp32 arithmetic, rounded to bf16) straight into their slots with 16-byte stores.
 // Nothing else in the cache is written.
+//
+// Into a quantised cache (PagedKVCacheCollection's scale_dtype_ / quantization_granularity_)
+// the rounded bf16 values of each 128-column block are quantised on the spot, the block
+// being the 16 chunks of one half-warp: s = amax / 448 (fp32), codes e4m3_rne_satfinite(y / s)
+// with the division in fp32, correctly rounded; the slot gets the codes, the bf16 rope
+// columns and the scales.
 #include "pkm_device.cuh"
 #include "pkm_internal.h"
 
@@ -96,8 +102,9 @@ __device__ __forceinline__ uint32_t rows_bytes_of(int64_t r0, int64_t total_rows
     return static_cast<uint32_t>(rows * C * 2);
 }
 
-// NC = 16-byte chunks of the normalised part per lane (ceil(R / 256)).
-template <int NC>
+// NC = 16-byte chunks of the normalised part per lane (ceil(R / 256)).  QUANT: the
+// destination is a quantised cache (codes, bf16 rope, fp32 block scales per slot).
+template <int NC, bool QUANT>
 __global__ void __launch_bounds__(kThreads, 1)
     cache_write_kernel(const CacheWriteArgs a, int32_t stages, StageLayout L) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -232,8 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         report(a.status, PKM_ERR_OUT_OF_RANGE);
                     continue;
                 }
-                uint16_t* dst = a.cache_layer + static_cast<int64_t>(page[u]) * a.page_stride +
-                                static_cast<int64_t>(slot[u]) * a.slot_stride;
+                const int64_t doff = static_cast<int64_t>(page[u]) * a.page_stride +
+                                     static_cast<int64_t>(slot[u]) * a.slot_stride;
+                uint16_t* dst = QUANT ? nullptr : a.cache_layer + doff;
+                uint8_t* dstq = QUANT ? a.qcache_layer + doff : nullptr;
                 float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
                 for (int j = 0; j < NC; ++j) {
@@ -247,8 +256,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int sh = 16; sh >= 1; sh >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, sh);
                 const float inv = rsqrtf(fmaf(ss, inv_r, a.epsilon));
+                if constexpr (QUANT) {
+                    // round to bf16 as the bf16 cache would, then quantise each 128-column
+                    // block (16 chunks = one half-warp): s = amax / 448, q = e4m3(y / s)
 #pragma unroll
-                for (int j = 0; j < NC; ++j) {
+                    for (int j = 0; j < NC; ++j) {
+                        const int c = lane + 32 * j;
+                        float f[8], y[8];
+                        unpack8(nv[u][j], f);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float g0, g1, y0, y1;
+                            mul2(g0, g1, gr[j][2 * i], gr[j][2 * i + 1], inv, inv);
+                            mul2(y0, y1, f[2 * i], f[2 * i + 1], g0, g1);
+                            const uint32_t pk = pack_bf16x2(y0, y1);
+                            y[2 * i] = __uint_as_float(pk << 16);
+                            y[2 * i + 1] = __uint_as_float(pk & 0xFFFF0000u);
+                        }
+                        float amax = 0.0f;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(y[i]));
+#pragma unroll
+                        for (int sh = 8; sh >= 1; sh >>= 1)
+                            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
+                        const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+                        if (c < nope_chunks) {
+                            const uint32_t lo =
+                                e4m3x2(__fdiv_rn(y[0], s), __fdiv_rn(y[1], s)) |
+                                (e4m3x2(__fdiv_rn(y[2], s), __fdiv_rn(y[3], s)) << 16);
+                            const uint32_t hi =
+                                e4m3x2(__fdiv_rn(y[4], s), __fdiv_rn(y[5], s)) |
+                                (e4m3x2(__fdiv_rn(y[6], s), __fdiv_rn(y[7], s)) << 16);
+                            *reinterpret_cast<uint2*>(dstq + c * 8) = make_uint2(lo, hi);
+                            if ((lane & 15) == 0)
+                                *reinterpret_cast<float*>(dstq + R + 2 * P + 4 * (c / 16)) = s;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < NC && !QUANT; ++j) {
                     const int c = lane + 32 * j;
                     if (c >= nope_chunks) break;
                     float f[8];
@@ -277,7 +323,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float c = cs[2 * i], s = cs[2 * i + 1];
                         o[i] = pack_bf16x2(fmaf(x0, c, -x1 * s), fmaf(x0, s, x1 * c));
                     }
-                    st_v4(dst + R + lane * 8, make_uint4(o[0], o[1], o[2], o[3]));
+                    if constexpr (QUANT)
+                        st_v4(dstq + R + lane * 16, make_uint4(o[0], o[1], o[2], o[3]));
+                    else
+                        st_v4(dst + R + lane * 8, make_uint4(o[0], o[1], o[2], o[3]));
                 }
             }
         }
@@ -297,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 uint32_t round16(uint32_t v) { return (v + 15u) & ~15u; }
 
-template <int NC>
+template <int NC, bool QUANT>
 cudaError_t launch_nc(const CacheWriteArgs& args, int num_sms, cudaStream_t stream) {
     const uint32_t C = static_cast<uint32_t>(args.kv_lora_rank + args.rope_dim);
     StageLayout L;
@@ -309,25 +358,31 @@ cudaError_t launch_nc(const CacheWriteArgs& args, int num_sms, cudaStream_t stre
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) stages = 2;
     const size_t smem = static_cast<size_t>(stages) * L.bytes;
-    cudaError_t e = cudaFuncSetAttribute(cache_write_kernel<NC>,
+    cudaError_t e = cudaFuncSetAttribute(cache_write_kernel<NC, QUANT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t n_chunks = (static_cast<int64_t>(args.total_rows) + kChunkRows - 1) / kChunkRows;
     int64_t blocks = n_chunks < num_sms ? n_chunks : num_sms;
     if (blocks < 1) blocks = 1;
-    cache_write_kernel<NC><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(args, stages, L);
+    cache_write_kernel<NC, QUANT><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(
+        args, stages, L);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_cache_write(CacheWriteArgs args, int num_sms, cudaStream_t stream) {
+    const bool q = args.qcache_layer != nullptr;
     switch ((args.kv_lora_rank / 8 + 31) / 32) {
-        case 1: return launch_nc<1>(args, num_sms, stream);
-        case 2: return launch_nc<2>(args, num_sms, stream);
-        case 3: return launch_nc<3>(args, num_sms, stream);
-        default: return launch_nc<4>(args, num_sms, stream);
+        case 1: return q ? launch_nc<1, true>(args, num_sms, stream)
+                         : launch_nc<1, false>(args, num_sms, stream);
+        case 2: return q ? launch_nc<2, true>(args, num_sms, stream)
+                         : launch_nc<2, false>(args, num_sms, stream);
+        case 3: return q ? launch_nc<3, true>(args, num_sms, stream)
+                         : launch_nc<3, false>(args, num_sms, stream);
+        default: return q ? launch_nc<4, true>(args, num_sms, stream)
+                          : launch_nc<4, false>(args, num_sms, stream);
     }
 }
 

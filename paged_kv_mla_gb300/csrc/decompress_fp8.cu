@@ -25,6 +25,8 @@
 //      k_buffer in whole 128-byte row segments (through a swizzled 4 KB shared buffer per
 //      warp).  The accumulators go back to the MMAs once per tile, right after the last
 //      k-block is read, so the rounding and stores overlap the next tile's MMAs.
+#include <cuda_fp16.h>
+
 #include "pkm_device.cuh"
 #include "pkm_internal.h"
 
@@ -34,12 +36,6 @@ namespace {
 // ------------------------------------------------------------------------------------
 // 1. gather + quantise
 // ------------------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;  // lo in the low byte
-}
 
 __global__ void __launch_bounds__(256)
     fp8_gather_quantize_kernel(const DecompressArgs a, const Fp8Extra x) {
@@ -92,6 +88,66 @@ __global__ void __launch_bounds__(256)
         }
         for (int c = nope_chunks + lane; c < all_chunks; c += 32)
             st_v4(lat + c * 8, ld_nc_v4(src + c * 8));
+    }
+}
+
+// 1b. gather from a quantised cache: the slot already holds the codes and the block
+// scales, so they are copied as they are; k_latent (optional) gets the dequantised nope
+// values fl32(e4m3 * scale) rounded to bf16 and the rope columns bit for bit.
+
+// Two e4m3 codes (first in the low byte) to fp32, exactly (e4m3 is a subset of f16).
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t two, float& lo, float& hi) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two)));
+    lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+    hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+}
+
+__global__ void __launch_bounds__(256)
+    fp8_gather_qcache_kernel(const DecompressArgs a, const Fp8Extra x) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t row_end = decompress_row_end(a);
+    const int R = a.kv_lora_rank;
+    const int C = a.latent_cols;
+    const int P = C - R;
+    const int code_chunks = R / 16;  // 16 codes per 16-byte chunk
+    const int rope_chunks = P / 8;   // 8 bf16 values per 16-byte chunk
+    const int kblocks = R / 128;
+    for (int64_t r = warp_id; r < row_end; r += nwarps) {
+        const int64_t off = decompress_row_source(a, r, row_end);
+        if (off < 0) {
+            if (off == -2 && lane == 0) report(a.status, PKM_ERR_OUT_OF_RANGE);
+            continue;
+        }
+        const uint8_t* slot = a.qcache_layer + off;
+        const float* scales = reinterpret_cast<const float*>(slot + R + 2 * P);
+        uint8_t* qrow = x.q_latent + r * R;
+        for (int c = lane; c < code_chunks; c += 32) {
+            const uint4 v = ld_nc_v4(slot + c * 16);
+            st_v4(qrow + c * 16, v);
+            if (a.k_latent != nullptr) {
+                const float s = __ldg(scales + c / 8);  // 8 chunks = one 128-column block
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t o[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float f0, f1, f2, f3;
+                    e4m3x2_to_f32(w[i] & 0xFFFFu, f0, f1);
+                    e4m3x2_to_f32(w[i] >> 16, f2, f3);
+                    o[2 * i] = pack_bf16x2(__fmul_rn(f0, s), __fmul_rn(f1, s));
+                    o[2 * i + 1] = pack_bf16x2(__fmul_rn(f2, s), __fmul_rn(f3, s));
+                }
+                uint16_t* lat = a.k_latent + r * C + c * 16;
+                st_v4(lat, make_uint4(o[0], o[1], o[2], o[3]));
+                st_v4(lat + 8, make_uint4(o[4], o[5], o[6], o[7]));
+            }
+        }
+        if (lane < kblocks) x.q_scale[r * kblocks + lane] = __ldg(scales + lane);
+        if (a.k_latent != nullptr)
+            for (int c = lane; c < rope_chunks; c += 32)
+                st_v4(a.k_latent + r * C + R + c * 8, ld_nc_v4(slot + R + c * 16));
     }
 }
 
@@ -441,6 +497,17 @@ cudaError_t launch_fp8_gather_quantize(DecompressArgs args, Fp8Extra extra, int 
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     fp8_gather_quantize_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(args, extra);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_gather_qcache(DecompressArgs args, Fp8Extra extra, int num_sms,
+                                     cudaStream_t stream) {
+    const int64_t rows = args.buffer_length;
+    int64_t blocks = (rows + 7) / 8;  // 8 warps (rows in flight) per block
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    fp8_gather_qcache_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(args, extra);
     return cudaGetLastError();
 }
 

@@ -472,6 +472,13 @@ __device__ __forceinline__ void warp_store_rows_32x64(uint32_t stage, const uint
     __syncwarp();  // the box may be overwritten once every lane has read its part
 }
 
+// Two fp32 values to e4m3 (round to nearest even, saturating to +-448); lo in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // (d0, d1) += (a0, a1) * (b0, b1), one packed fp32x2 FMA (each lane rounded as fmaf).
 __device__ __forceinline__ void fma2v(float& d0, float& d1, float a0, float a1, float b0,
                                       float b1) {

@@ -12,8 +12,9 @@ namespace pkm {
 // One decompress problem, already validated on the host.  Pointers are device memory.
 struct DecompressArgs {
     const uint16_t* cache_layer;   // cache data + layer_idx * layer_stride (bf16)
-    int64_t page_stride;           // elements
-    int64_t slot_stride;           // elements
+    const uint8_t* qcache_layer;   // or: a quantised cache's layer (strides then in bytes)
+    int64_t page_stride;           // elements (bytes for a quantised cache)
+    int64_t slot_stride;           // elements (bytes for a quantised cache)
     int32_t num_pages;
     int32_t page_size;
     int32_t max_pages;             // page-table row length
@@ -66,6 +67,7 @@ struct CacheWriteArgs {
     const uint32_t* cache_lengths;
     int32_t* status;
     uint64_t timeout_ns;
+    uint8_t* qcache_layer;         // quantised destination (byte strides), or null
 };
 
 // One kv_matmul problem, already validated.
@@ -95,6 +97,8 @@ cudaError_t launch_decompress_bf16(const CUtensorMap& tm_w, const CUtensorMap& t
                                    cudaStream_t stream);
 cudaError_t launch_fp8_gather_quantize(DecompressArgs args, Fp8Extra extra, int num_sms,
                                        cudaStream_t stream);
+cudaError_t launch_fp8_gather_qcache(DecompressArgs args, Fp8Extra extra, int num_sms,
+                                     cudaStream_t stream);
 cudaError_t launch_decompress_fp8_gemm(const CUtensorMap& tm_q, const CUtensorMap& tm_w,
                                        const CUtensorMap& tm_wv, DecompressArgs args,
                                        Fp8Extra extra, int num_sms, cudaStream_t stream);

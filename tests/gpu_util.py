@@ -50,7 +50,7 @@ def assert_close_bf16(got_bits, ref_bits, tol, what=""):
 class DeviceDecompress:
     """A DecompressInputs problem resident on the GPU, with sentinel-filled outputs."""
 
-    def __init__(self, d: DecompressInputs, fp8: bool = False):
+    def __init__(self, d: DecompressInputs, fp8: bool = False, with_latent: bool = True):
         import paged_kv_mla_gb300 as pkm
         self.d = d
         self.cache = dev(d.cache)
@@ -58,10 +58,18 @@ class DeviceDecompress:
         self.bro = dev(d.buffer_row_offsets)
         self.co = dev(d.cache_offsets)
         ls, ps, ss = d.strides
-        self.pc = pkm.PagedCache(data=self.cache, page_table=self.pt, layer_stride=ls,
-                                 page_stride=ps, slot_stride=ss, num_layers=d.num_layers,
-                                 num_pages=d.num_pages, page_size=d.page_size,
-                                 row_elems=d.latent_cols)
+        self.with_latent = with_latent
+        if d.quantised:     # a quantised cache is only read by the FP8 path
+            fp8 = True
+            self.qc = pkm.QuantCache(data=self.cache, page_table=self.pt, layer_stride=ls,
+                                     page_stride=ps, slot_stride=ss, num_layers=d.num_layers,
+                                     num_pages=d.num_pages, page_size=d.page_size,
+                                     kv_lora_rank=d.kv_lora_rank, rope_dim=d.rope_dim)
+        else:
+            self.pc = pkm.PagedCache(data=self.cache, page_table=self.pt, layer_stride=ls,
+                                     page_stride=ps, slot_stride=ss, num_layers=d.num_layers,
+                                     num_pages=d.num_pages, page_size=d.page_size,
+                                     row_elems=d.latent_cols)
         L = max(d.buffer_length, 1)
         self.k_latent = torch.full((L, d.latent_cols), _i16(SENTINEL_OUT), dtype=torch.int16,
                                    device="cuda")
@@ -88,6 +96,11 @@ class DeviceDecompress:
     def run(self, stream=None, check=True):
         import paged_kv_mla_gb300 as pkm
         d = self.d
+        if d.quantised:
+            return pkm.mla_decompress_k_paged_fp8_qcache(
+                self.qc, d.layer_idx, self.bro, self.co, d.buffer_length, self.w, self.w_scale,
+                self.k_latent if self.with_latent else None, self.k_buffer, self.workspace,
+                dev_status=self.status, stream=stream, check=check)
         if self.w_uv is not None and self.fp8:
             return pkm.mla_decompress_kv_paged_fp8(
                 self.pc, d.layer_idx, self.bro, self.co, d.buffer_length, d.kv_lora_rank,
@@ -164,19 +177,32 @@ class DeviceCacheWrite:
         self.pt = dev(c.page_table)
         self.cl = dev(c.cache_lengths)
         ls, ps, ss = c.strides
-        self.pc = pkm.PagedCache(data=self.cache, page_table=self.pt, layer_stride=ls,
-                                 page_stride=ps, slot_stride=ss, num_layers=c.cache.shape[0],
-                                 num_pages=c.num_pages, page_size=c.page_size,
-                                 row_elems=c.row_elems, cache_lengths=self.cl)
+        if c.quantised:
+            self.qc = pkm.QuantCache(data=self.cache, page_table=self.pt, layer_stride=ls,
+                                     page_stride=ps, slot_stride=ss, num_layers=c.cache.shape[0],
+                                     num_pages=c.num_pages, page_size=c.page_size,
+                                     kv_lora_rank=c.kv_lora_rank, rope_dim=c.rope_dim,
+                                     cache_lengths=self.cl)
+        else:
+            self.pc = pkm.PagedCache(data=self.cache, page_table=self.pt, layer_stride=ls,
+                                     page_stride=ps, slot_stride=ss, num_layers=c.cache.shape[0],
+                                     num_pages=c.num_pages, page_size=c.page_size,
+                                     row_elems=c.row_elems, cache_lengths=self.cl)
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
 
     def run(self, stream=None, check=True):
         import paged_kv_mla_gb300 as pkm
         c = self.c
+        if c.quantised:
+            return pkm.mla_cache_write_paged_qcache(self.latent, self.iro, self.gamma, c.epsilon,
+                                                    self.freqs, self.qc, c.layer_idx,
+                                                    dev_status=self.status, stream=stream,
+                                                    check=check)
         return pkm.mla_cache_write_paged(self.latent, self.iro, self.gamma, c.epsilon, self.freqs,
                                          self.pc, c.layer_idx, c.kv_lora_rank, c.rope_dim,
                                          dev_status=self.status, stream=stream, check=check)
 
     def results(self):
         torch.cuda.synchronize()
-        return host_u16(self.cache).reshape(self.c.cache.shape), int(self.status.item())
+        out = self.cache.cpu().numpy() if self.c.quantised else host_u16(self.cache)
+        return out.reshape(self.c.cache.shape), int(self.status.item())

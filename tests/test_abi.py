@@ -34,6 +34,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ["mla_decompress_k_paged", "mla_decompress_k_paged_fp8", "mla_decompress_kv_paged",
               "mla_decompress_kv_paged_fp8", "mla_cache_write_paged",
+              "mla_decompress_k_paged_fp8_qcache", "mla_cache_write_paged_qcache",
               "mla_decompress_k_paged_fp8_workspace_size", "kv_matmul_paged", "pkm_status_string"]:
         assert n in names
 
@@ -124,6 +125,35 @@ def test_invalid_calls_return_status_without_a_gpu(lib):
     assert call_cw(gamma=torch.ones(65, dtype=torch.float32)[1:]) == pkm.PKM_ERR_INVALID_ARG  # misaligned gamma
     assert call_cw(cache=_cache(pkm, cache_lengths=co, slot_stride=81)) == pkm.PKM_ERR_INVALID_ARG
     assert call_cw(lat=lat[:0]) == pkm.PKM_OK                           # no new rows
+    # quantised cache: byte strides, payload and R rules are checked on the host
+    def qc(**kw):
+        base = dict(data=torch.zeros(4096, dtype=torch.uint8), page_table=torch.zeros(8, dtype=torch.int32),
+                    layer_stride=16 * 160, page_stride=16 * 160, slot_stride=160, num_layers=1,
+                    num_pages=1, page_size=16, kv_lora_rank=128, rope_dim=8, cache_lengths=co)
+        base.update(kw)
+        return pkm.QuantCache(**base)
+    w8 = torch.zeros(128 * 128, dtype=torch.uint8).view(128, 128)
+    ws = torch.ones(1, dtype=torch.float32)
+    wsp = torch.zeros(1 << 16, dtype=torch.uint8)
+
+    def call_qd(cache, w=w8, kl=None, L=4):
+        return pkm.mla_decompress_k_paged_fp8_qcache(cache, 0, bro, co, L, w, ws, kl, t16, wsp,
+                                                     stream=0, check=False)
+    assert call_qd(qc(slot_stride=144)) == pkm.PKM_ERR_INVALID_ARG      # below the 148-byte payload
+    assert call_qd(qc(slot_stride=168)) == pkm.PKM_ERR_INVALID_ARG      # not a multiple of 16
+    assert call_qd(qc(kv_lora_rank=64, slot_stride=96)) == pkm.PKM_ERR_UNSUPPORTED
+    assert call_qd(qc(), kl=t16[1:]) == pkm.PKM_ERR_INVALID_ARG          # misaligned k_latent
+    assert call_qd(qc(), L=0) == pkm.PKM_OK
+    lq = torch.zeros(4, 136, dtype=torch.int16)
+    fq = torch.zeros(32, 8, dtype=torch.float32)
+    g128 = torch.ones(128, dtype=torch.float32)
+
+    def call_qw(cache):
+        return pkm.mla_cache_write_paged_qcache(lq, bro, g128, 1e-6, fq, cache, 0, stream=0,
+                                                check=False)
+    assert call_qw(qc(kv_lora_rank=256, slot_stride=272)) == pkm.PKM_ERR_INVALID_ARG  # payload 280
+    assert call_qw(qc(kv_lora_rank=192, slot_stride=224)) == pkm.PKM_ERR_UNSUPPORTED  # R % 128
+    assert call_qw(qc(cache_lengths=None)) == pkm.PKM_ERR_INVALID_ARG
 
 
 def test_oracle_and_product_share_no_code():

@@ -31,7 +31,7 @@ def _worker(rank, world, port, out):
 
 def test_two_rank_timing_is_max_and_rate_counts_both_replicas():
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.start_processes(_worker, args=(2, port, out), nprocs=2, join=True, start_method="spawn")
     assert out[0] == out[1]

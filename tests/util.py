@@ -84,5 +84,28 @@ def oracle_cache_write(c: CacheWriteInputs):
     return st, view.data.reshape(c.cache.shape)
 
 
+def qcache_view(d, data=None) -> oracle.QuantCacheView:
+    """Oracle view of a quantised cache (DecompressInputs or CacheWriteInputs)."""
+    ls, ps, ss = d.strides
+    return oracle.QuantCacheView(d.cache if data is None else data, ls, ps, ss, d.num_pages,
+                                 d.page_size, d.page_table, d.page_table.shape[1])
+
+
+def oracle_decompress_qcache(d: DecompressInputs):
+    return oracle.decompress_k_qcache_fp8(qcache_view(d), d.layer_idx, d.buffer_row_offsets,
+                                          d.cache_offsets, d.batch, d.buffer_length,
+                                          d.kv_lora_rank, d.rope_dim, d.w_k_e4m3, d.w_k_scale)
+
+
+def oracle_cache_write_q(c: CacheWriteInputs):
+    """Runs the quantised cache-write oracle on a copy of the cache; returns (status,
+    cache_after)."""
+    view = qcache_view(c, c.cache.copy())
+    st = oracle.cache_write_q(c.latent, c.input_row_offsets, c.batch, c.total_rows,
+                              c.kv_lora_rank, c.rope_dim, c.gamma, c.epsilon, c.freqs_cis, view,
+                              c.cache_lengths, c.layer_idx)
+    return st, view.data.reshape(c.cache.shape)
+
+
 def e4m3_decode_table() -> np.ndarray:
     return np.array([oracle.e4m3_to_double(c) for c in range(256)], np.float64)
