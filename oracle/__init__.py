@@ -13,7 +13,8 @@ Each wrapper follows the passage cited in the C source:
     (the cache-write side)
   * PagedKVCacheCollection[..., scale_dtype_, quantization_granularity_] -- the quantised
     paged latent cache (written by the cache-write side, read by the FP8 decompress)
-  * kv_matmul_ragged_paged -- Args (hidden_state, input_row_offsets, weight, kv_collection)
+  * kv_matmul_ragged_paged -- Args (hidden_state, input_row_offsets, weight, kv_collection),
+    and its FP8 form with the scale-granularity parameters of mla_prefill_decode_graph_fp8
 """
 from __future__ import annotations
 
@@ -122,6 +123,10 @@ def lib():
                                            _i64, _i64, _i64, _i32, _i32, _i32, _u32p, _i32, _u32p,
                                            _u32]
             L.oracle_kv_matmul.restype = ctypes.c_int
+            L.oracle_kv_matmul_fp8.argtypes = [_u16p, _u32p, _i32, _i32, _i32, _u8p, _f32p, _i32,
+                                               _u16p, _i64, _i64, _i64, _i64, _i32, _i32, _i32,
+                                               _u32p, _i32, _u32p, _u32, _u8p, _f32p]
+            L.oracle_kv_matmul_fp8.restype = ctypes.c_int
             _i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
             L.oracle_kv_row_dest.argtypes = [_u32p, _i32, _i32, _u32p, _u32p, _i32, _i32, _i32, _i64,
                                              _i64, _i64p]
@@ -497,6 +502,28 @@ def kv_matmul(hidden_state, input_row_offsets, batch, total_rows, weight, cache:
                                   cache.num_pages, cache.page_size, int(head_elems),
                                   cache.page_table, cache.max_pages_per_seq,
                                   _c(cache_lengths, np.uint32), int(layer_idx))
+
+
+def kv_matmul_fp8(hidden_state, input_row_offsets, batch, total_rows, w_e4m3, w_scale,
+                  cache: PagedCacheView, head_elems, cache_lengths, layer_idx):
+    """FP8 kv_matmul into the paged cache (cache.data modified in place).  Returns (status,
+    q [total_rows, k_in], s [total_rows, k_in/128]) with the quantised rows that were
+    written (zeros elsewhere)."""
+    hidden_state = _c(hidden_state, np.uint16)
+    w_e4m3 = _c(w_e4m3, np.uint8)
+    n_out, k_in = w_e4m3.shape
+    M1 = max(int(total_rows), 1)
+    q = np.zeros((M1, k_in), np.uint8)
+    s = np.zeros((M1, k_in // 128), np.float32)
+    st = lib().oracle_kv_matmul_fp8(hidden_state.reshape(-1) if total_rows else np.zeros(1, np.uint16),
+                                    _c(input_row_offsets, np.uint32), int(batch), int(total_rows),
+                                    k_in, w_e4m3.reshape(-1), _c(w_scale, np.float32).reshape(-1),
+                                    n_out, cache.data, cache.layer_stride, cache.page_stride,
+                                    cache.slot_stride, cache.kv_stride, cache.num_pages,
+                                    cache.page_size, int(head_elems), cache.page_table,
+                                    cache.max_pages_per_seq, _c(cache_lengths, np.uint32),
+                                    int(layer_idx), q.reshape(-1), s.reshape(-1))
+    return st, q[:total_rows], s[:total_rows]
 
 
 def kv_row_dest(input_row_offsets, batch, total_rows, cache_lengths, cache: PagedCacheView):

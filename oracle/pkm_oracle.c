@@ -25,7 +25,8 @@
  *     latent cache, written by the cache-write side and read by the FP8 decompress.
  *   - kv_matmul_ragged_paged (Modular MAX kernels, nn/kv_cache_ragged), Args: a GEMM on
  *     the ragged hidden_state whose rows are written into the paged cache of one layer,
- *     after each request's existing cache length.
+ *     after each request's existing cache length.  Its FP8 form takes the fp8
+ *     type and m/n/k scale granularities of mla_prefill_decode_graph_fp8.
  *
  * Arithmetic: fp64 accumulation; the only roundings are the final fp64 -> bf16
  * round-to-nearest-even, and (FP8 path) the activation quantisation, which is taken in
@@ -836,6 +837,59 @@ int oracle_kv_matmul(const uint16_t* hidden_state, const uint32_t* input_row_off
                            oracle_bf16_to_double(weight[k * n_out + n]);
                 int64_t plane = (n < head_elems) ? 0 : kv_stride;
                 layer[plane + off + (n % head_elems)] = oracle_double_to_bf16(acc);
+            }
+        }
+    }
+    return status;
+}
+
+/*
+ * FP8 kv_matmul with block scales (kv_matmul_ragged_paged's GEMM and scatter, with the FP8
+ * type and scale-granularity parameters of mla_prefill_decode_graph_fp8: fp8_dtype,
+ * fp8_scale_dtype, m/n/k_scale_granularity).  Readings: the hidden state still arrives in
+ * bf16 and is quantised per token per 128-column block exactly as the FP8 decompress
+ * quantises the latent (oracle_quantize_row_e4m3: s = amax/448, q = e4m3_rne(x / s));
+ * the weight is given quantised, e4m3 [n_out, k_in] (k_in contiguous, the transpose of the
+ * bf16 weight's [k_in, n_out]) with fp32 scales [n_out/128, k_in/128];
+ *   Y[r, n] = bf16( sum_kb sx[r, kb] * sw[n/128, kb] * sum_{k in kb} qx[r, k] * qw[n, k] )
+ * in fp64 on the dequantised values (fp8_row_product), stored like oracle_kv_matmul.
+ * q_out [total_rows, k_in] and s_out [total_rows, k_in/128] (optional) receive the
+ * quantised rows that were written.  Returns 0 or 4 as oracle_kv_matmul does.
+ */
+int oracle_kv_matmul_fp8(const uint16_t* hidden_state, const uint32_t* input_row_offsets,
+                         int32_t batch, int32_t total_rows, int32_t k_in, const uint8_t* w_e4m3,
+                         const float* w_scale, int32_t n_out, uint16_t* cache,
+                         int64_t layer_stride, int64_t page_stride, int64_t slot_stride,
+                         int64_t kv_stride, int32_t num_pages, int32_t page_size,
+                         int32_t head_elems, const uint32_t* page_table,
+                         int32_t max_pages_per_seq, const uint32_t* cache_lengths,
+                         uint32_t layer_idx, uint8_t* q_out, float* s_out) {
+    int status = 0;
+    uint16_t* layer = cache + (int64_t)layer_idx * layer_stride;
+    uint8_t q[8192];
+    float sx[64];
+    uint16_t y[8192];
+    if (k_in > 8192 || n_out > 8192) return 1;
+    for (int32_t b = 0; b < batch; ++b) {
+        uint32_t begin = input_row_offsets[b];
+        uint32_t end = input_row_offsets[b + 1];
+        for (uint32_t i = 0; begin + i < end; ++i) {
+            uint64_t r = (uint64_t)begin + i;
+            if (r >= (uint64_t)total_rows) break;
+            uint64_t pos = (uint64_t)cache_lengths[b] + i;
+            int64_t off = token_offset(page_table, max_pages_per_seq, num_pages, page_size,
+                                       page_stride, slot_stride, b, pos);
+            if (off < 0) {
+                status = 4;
+                continue;
+            }
+            oracle_quantize_row_e4m3(hidden_state + r * (uint64_t)k_in, k_in, q, sx);
+            if (q_out) memcpy(q_out + r * (uint64_t)k_in, q, (size_t)k_in);
+            if (s_out) memcpy(s_out + r * (uint64_t)(k_in / 128), sx, sizeof(float) * (size_t)(k_in / 128));
+            fp8_row_product(q, sx, w_e4m3, w_scale, k_in, n_out, y);
+            for (int64_t n = 0; n < n_out; ++n) {
+                int64_t plane = (n < head_elems) ? 0 : kv_stride;
+                layer[plane + off + (n % head_elems)] = y[n];
             }
         }
     }

@@ -426,6 +426,12 @@ class KvMatmulInputs:
     head_elems: int
     layer_idx: int
     new_tokens: Optional[np.ndarray] = None
+    w_e4m3: Optional[np.ndarray] = None   # FP8 form: uint8 [n_out, k_in] (weight is then None)
+    w_scale: Optional[np.ndarray] = None  # float32 [n_out/128, k_in/128]
+
+    @property
+    def fp8(self) -> bool:
+        return self.w_e4m3 is not None
 
     @property
     def batch(self) -> int:
@@ -437,11 +443,11 @@ class KvMatmulInputs:
 
     @property
     def k_in(self) -> int:
-        return int(self.weight.shape[0])
+        return int(self.w_e4m3.shape[1] if self.fp8 else self.weight.shape[0])
 
     @property
     def n_out(self) -> int:
-        return int(self.weight.shape[1])
+        return int(self.w_e4m3.shape[0] if self.fp8 else self.weight.shape[1])
 
     @property
     def num_pages(self) -> int:
@@ -463,14 +469,20 @@ class KvMatmulInputs:
 
     @property
     def bytes_moved(self) -> int:
-        """Algorithmic HBM bytes: read hidden_state and weight once, write every output."""
+        """Algorithmic HBM bytes: read hidden_state and weight once, write every output; the
+        FP8 form also writes and reads back the quantised rows (k_in + k_in/32 bytes a row)
+        and reads an e4m3 weight with its scales."""
+        if self.fp8:
+            q = self.total_rows * (self.k_in + self.k_in // 32)
+            return (2 * self.total_rows * self.k_in + 2 * q + self.w_e4m3.nbytes +
+                    self.w_scale.nbytes + 2 * self.total_rows * self.n_out)
         return 2 * (self.total_rows * self.k_in + self.k_in * self.n_out +
                     self.total_rows * self.n_out)
 
 
 def make_kv_matmul(name, seed, new_tokens, cache_lengths, k_in, num_kv_heads, head_dim,
                    page_size, num_layers=1, layer_idx=0, k_only=False, extra_pages=0,
-                   int_values=False, w_std=None) -> KvMatmulInputs:
+                   int_values=False, w_std=None, fp8=False) -> KvMatmulInputs:
     g = _gen(seed)
     new_tokens = np.asarray(new_tokens, np.int64)
     cache_lengths = np.asarray(cache_lengths, np.int64)
@@ -492,19 +504,29 @@ def make_kv_matmul(name, seed, new_tokens, cache_lengths, k_in, num_kv_heads, he
     cache = np.empty((num_layers, 2, total_pages, page_size, HD), np.uint16)
     cache[:, 0] = SENTINEL_K
     cache[:, 1] = SENTINEL_V
-    return KvMatmulInputs(name=name, hidden_state=hidden, input_row_offsets=iro, weight=weight,
-                          cache=cache, page_table=pt, cache_lengths=cache_lengths.astype(np.uint32),
-                          head_elems=HD, layer_idx=layer_idx, new_tokens=new_tokens)
+    k = KvMatmulInputs(name=name, hidden_state=hidden, input_row_offsets=iro, weight=weight,
+                       cache=cache, page_table=pt, cache_lengths=cache_lengths.astype(np.uint32),
+                       head_elems=HD, layer_idx=layer_idx, new_tokens=new_tokens)
+    if fp8:
+        # the FP8 form: a weight drawn in fp32 as [n_out, k_in] and quantised per 128 x 128
+        # block like the FP8 decompress weights (its own generator: the rest is unchanged)
+        gw = _gen(seed + 7717)
+        std = w_std if w_std is not None else 1.0 / math.sqrt(k_in)
+        w = torch.randn(n_out, k_in, generator=gw, dtype=torch.float32) * std
+        k.w_e4m3, k.w_scale = quantize_weight_e4m3(w)
+        k.weight = None
+    return k
 
 
-def kv_matmul_write_path(seed=1004) -> KvMatmulInputs:
+def kv_matmul_write_path(seed=1004, fp8=False) -> KvMatmulInputs:
     """32 requests, new ~U[1,512], cache_len ~U[0,2048], hidden [sum(new), 4096] ~N(0,1),
-    weight [4096, 2048] ~N(0, 1/64), 8 kv heads x 128 (K then V), page_size 128."""
+    weight [4096, 2048] ~N(0, 1/64), 8 kv heads x 128 (K then V), page_size 128; the FP8
+    form has an e4m3 weight [2048, 4096] with 128 x 128 fp32 block scales."""
     g = _gen(seed)
     new = torch.randint(1, 513, (32,), generator=g).numpy()
     cl = torch.randint(0, 2049, (32,), generator=g).numpy()
-    return make_kv_matmul("kv_matmul_write_path", seed + 1, new, cl, 4096, 8, 128, 128,
-                          w_std=1.0 / 64)
+    return make_kv_matmul("kv_matmul_fp8_write_path" if fp8 else "kv_matmul_write_path",
+                          seed + 1, new, cl, 4096, 8, 128, 128, w_std=1.0 / 64, fp8=fp8)
 
 
 # Names used by tests and the benchmark.
@@ -516,6 +538,7 @@ WORKLOADS = {
     "deepseek_v3_bf16_decompress_kv": lambda: deepseek_decompress_kv(1001, fp8=False),
     "deepseek_v3_fp8_decompress_kv": lambda: deepseek_decompress_kv(1001, fp8=True),
     "kv_matmul_write_path": kv_matmul_write_path,
+    "kv_matmul_fp8_write_path": lambda: kv_matmul_write_path(1004, fp8=True),
     "cache_write_path": cache_write_path,
     "cache_write_q_path": lambda: cache_write_path(1007, quantised=True),
     "deepseek_v3_fp8_qcache_decompress": deepseek_qcache_decompress,
