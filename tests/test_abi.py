@@ -134,7 +134,8 @@ def test_invalid_calls_return_status_without_a_gpu(lib):
         return pkm.QuantCache(**base)
     w8 = torch.zeros(128 * 128, dtype=torch.uint8).view(128, 128)
     ws = torch.ones(1, dtype=torch.float32)
-    wsp = torch.zeros(1 << 16, dtype=torch.uint8)
+    wraw = torch.zeros((1 << 16) + 256, dtype=torch.uint8)
+    wsp = wraw[(-wraw.data_ptr()) % 256:][:1 << 16]                       # 256-byte aligned
 
     def call_qd(cache, w=w8, kl=None, L=4):
         return pkm.mla_decompress_k_paged_fp8_qcache(cache, 0, bro, co, L, w, ws, kl, t16, wsp,
