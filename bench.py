@@ -52,6 +52,7 @@ KERNEL_SOURCES = {
     "kv_matmul_kernel": ["kv_matmul.cu"],
     "cache_write_kernel": ["cache_write.cu"],
     "fp8_gather_qcache_kernel": ["decompress_fp8.cu"],
+    "kv_matmul_fp8_kernel": ["kv_matmul_fp8.cu"],
 }
 
 
@@ -337,6 +338,18 @@ def run_ours(args, rank, world, local_rank):
         "tflops": km.flops / tk / 1e12, "gbs": km.bytes_moved / tk / 1e9,
         "roofline_frac": t_roof / tk}
     del gk
+    kf = workloads.WORKLOADS["kv_matmul_fp8_write_path"]()
+    gf = DeviceKvMatmul(kf)
+    tf = _time_steps(gf.run, sec_steps, 3, flush, stream) / sec_steps
+    assert int(gf.status.item()) == 0
+    t_roof8 = max(kf.flops / (peaks["bf16_tflops"] * 2 * 1e12), kf.bytes_moved / (peaks["hbm_gbs"] * 1e9))
+    extra["kv_matmul_fp8"] = {
+        "workload": kf.name, "rows": kf.total_rows, "ms": tf * 1e3,
+        "tflops": kf.flops / tf / 1e12, "gbs": kf.bytes_moved / tf / 1e9,
+        "roofline_frac": t_roof8 / tf,
+        "roofline_peak": "fp8 = 2 x measured bf16 (the nominal dense ratio)",
+        "launches_per_step": 2}
+    del gf, kf
     from gpu_util import DeviceCacheWrite
     for key, wl in [("cache_write", "cache_write_path"), ("cache_write_q", "cache_write_q_path")]:
         cw = workloads.WORKLOADS[wl]()

@@ -417,6 +417,45 @@ pkm_status kv_matmul_paged(const void* hidden_state, const uint32_t* input_row_o
                            uint32_t layer_idx, int32_t* dev_status, void* stream);
 
 /*
+ * Bytes of device workspace kv_matmul_paged_fp8 needs for total_rows hidden rows of k_in
+ * columns (0 for invalid sizes).  Layout:
+ *     offset 0                                e4m3 codes [total_rows, k_in]
+ *     offset align256(total_rows * k_in)      fp32 scales [total_rows, k_in / 128]
+ */
+size_t kv_matmul_paged_fp8_workspace_size(int32_t total_rows, int32_t k_in);
+
+/*
+ * FP8 ragged GEMM with block scales, written into the paged K/V cache.
+ * Source: kv_matmul_ragged_paged (as for kv_matmul_paged) with the fp8 type and the
+ * m/n/k scale-granularity parameters of mla_prefill_decode_graph_fp8 (Parameters fp8_dtype,
+ * fp8_scale_dtype, m_scale_granularity, n_scale_granularity, k_scale_granularity), taken
+ * as m = 1, n = k = 128.
+ *
+ * The rows and positions of kv_matmul_paged.  Each hidden row is quantised per 128-column
+ * block like the FP8 decompress's latent (s = amax / 448 in fp32, 1 for an all-zero block;
+ * q = e4m3_rne_satfinite(x / s), the division in fp32), then
+ *     Y[r, n] = bf16( sum_kb s[r, kb] * w_scale[n / 128, kb]
+ *                      * sum_{k in kb} q[r, k] * w_e4m3[n, k] )
+ * goes to the K plane (n < HD) or the V plane (n >= HD) of position pos's slot.
+ *
+ *   hidden_state   device bf16 [total_rows, k_in], 16-byte aligned.
+ *   k_in           a multiple of 128.
+ *   w_e4m3         device e4m3 [n_out, k_in], k_in contiguous (the bf16 weight's
+ *                  transpose), 16-byte aligned.
+ *   w_scale        device fp32 [n_out / 128, k_in / 128], row-major.
+ *   n_out          HD or 2*HD, a multiple of 128; HD a multiple of 64.
+ *   workspace      device, >= kv_matmul_paged_fp8_workspace_size(total_rows, k_in) bytes,
+ *                  256-byte aligned; receives the quantised rows (layout above).
+ *   other arguments and errors as for kv_matmul_paged.
+ */
+pkm_status kv_matmul_paged_fp8(const void* hidden_state, const uint32_t* input_row_offsets,
+                               int32_t batch, int32_t total_rows, int32_t k_in,
+                               const void* w_e4m3, const float* w_scale, int32_t n_out,
+                               const pkm_paged_cache* kv_cache, uint32_t layer_idx,
+                               void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                               void* stream);
+
+/*
  * Failure-detection self check (no counterpart on the pages).  Launches one CTA that waits,
  * with the same bounded mbarrier wait every kernel above uses, on a barrier phase that
  * nothing completes.  After timeout_ms (1..5000) the wait gives up and PKM_ERR_TIMEOUT is

@@ -90,6 +90,11 @@ _lib.mla_decompress_kv_paged_fp8.restype = ctypes.c_int
 _lib.mla_cache_write_paged.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _vp, ctypes.c_float, _vp,
                                        _i32, ctypes.POINTER(_CCache), _u32, _vp, _vp]
 _lib.mla_cache_write_paged.restype = ctypes.c_int
+_lib.kv_matmul_paged_fp8_workspace_size.argtypes = [_i32, _i32]
+_lib.kv_matmul_paged_fp8_workspace_size.restype = _sz
+_lib.kv_matmul_paged_fp8.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32,
+                                     ctypes.POINTER(_CCache), _u32, _vp, _sz, _vp, _vp]
+_lib.kv_matmul_paged_fp8.restype = ctypes.c_int
 _lib.kv_matmul_paged.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _i32, ctypes.POINTER(_CCache),
                                  _u32, _vp, _vp]
 _lib.kv_matmul_paged.restype = ctypes.c_int
@@ -317,6 +322,28 @@ def mla_cache_write_paged(latent: torch.Tensor, input_row_offsets: torch.Tensor,
                                       int(freqs_cis.shape[0]), ctypes.byref(c), int(layer_idx),
                                       _ptr(dev_status), _stream(stream))
     return _check(code, "mla_cache_write_paged", check)
+
+
+def kv_matmul_paged_fp8_workspace_size(total_rows: int, k_in: int) -> int:
+    return int(_lib.kv_matmul_paged_fp8_workspace_size(int(total_rows), int(k_in)))
+
+
+def kv_matmul_paged_fp8(hidden_state: torch.Tensor, input_row_offsets: torch.Tensor,
+                        w_e4m3: torch.Tensor, w_scale: torch.Tensor, kv_cache: PagedCache,
+                        layer_idx: int, workspace: torch.Tensor,
+                        dev_status: Optional[torch.Tensor] = None, stream=None,
+                        check: bool = True) -> int:
+    """FP8 kv_matmul: hidden_state bf16 [M, k_in], w_e4m3 [n_out, k_in] with fp32 block scales
+    [n_out/128, k_in/128]; the quantised rows land in `workspace`."""
+    c = kv_cache.c_struct()
+    batch = int(input_row_offsets.shape[0]) - 1
+    code = _lib.kv_matmul_paged_fp8(_ptr(hidden_state), _ptr(input_row_offsets), batch,
+                                    int(hidden_state.shape[0]), int(hidden_state.shape[1]),
+                                    _ptr(w_e4m3), _ptr(w_scale), int(w_e4m3.shape[0]),
+                                    ctypes.byref(c), int(layer_idx), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _ptr(dev_status), _stream(stream))
+    return _check(code, "kv_matmul_paged_fp8", check)
 
 
 def mla_decompress_k_paged_fp8_noalloc(cache: PagedCache, layer_idx: int,

@@ -18,6 +18,7 @@ using pkm::DecompressArgs;
 using pkm::Fp8Extra;
 using pkm::CacheWriteArgs;
 using pkm::KvMatmulArgs;
+using pkm::KvFp8Extra;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool mult8(int64_t v) { return v >= 0 && (v % 8) == 0; }
@@ -675,6 +676,84 @@ pkm_status kv_matmul_paged(const void* hidden_state, const uint32_t* input_row_o
                    static_cast<uint64_t>(n_out) * 2, 64, 64))
         return PKM_ERR_CUDA;
     return pkm::launch_kv_matmul(tm_x, tm_w, a, sms, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PKM_OK
+               : PKM_ERR_CUDA;
+}
+
+size_t kv_matmul_paged_fp8_workspace_size(int32_t total_rows, int32_t k_in) {
+    if (total_rows < 0 || k_in <= 0 || k_in % 128 != 0) return 0;
+    const size_t M = static_cast<size_t>(total_rows), K = static_cast<size_t>(k_in);
+    return align256(M * K) + align256(M * (K / 128) * sizeof(float));
+}
+
+pkm_status kv_matmul_paged_fp8(const void* hidden_state, const uint32_t* input_row_offsets,
+                               int32_t batch, int32_t total_rows, int32_t k_in,
+                               const void* w_e4m3, const float* w_scale, int32_t n_out,
+                               const pkm_paged_cache* kv_cache, uint32_t layer_idx,
+                               void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                               void* stream) {
+    if (batch < 0 || total_rows < 0 || k_in <= 0 || n_out <= 0) return PKM_ERR_INVALID_ARG;
+    if (total_rows == 0 || batch == 0) return PKM_OK;
+    if (hidden_state == nullptr || input_row_offsets == nullptr || w_e4m3 == nullptr ||
+        w_scale == nullptr || workspace == nullptr || kv_cache == nullptr ||
+        kv_cache->data == nullptr || kv_cache->page_table == nullptr ||
+        kv_cache->cache_lengths == nullptr)
+        return PKM_ERR_INVALID_ARG;
+    if (kv_cache->num_layers <= 0 || layer_idx >= static_cast<uint32_t>(kv_cache->num_layers) ||
+        kv_cache->num_pages <= 0 || kv_cache->page_size <= 0 ||
+        kv_cache->max_pages_per_seq <= 0 || kv_cache->row_elems <= 0)
+        return PKM_ERR_INVALID_ARG;
+    const int32_t hd = kv_cache->row_elems;
+    if (n_out != hd && n_out != 2 * hd) return PKM_ERR_INVALID_ARG;
+    if (!mult8(kv_cache->layer_stride) || !mult8(kv_cache->page_stride) ||
+        !mult8(kv_cache->slot_stride) || !mult8(kv_cache->kv_stride))
+        return PKM_ERR_INVALID_ARG;
+    if (!aligned16(hidden_state) || !aligned16(w_e4m3) || !aligned16(kv_cache->data) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return PKM_ERR_INVALID_ARG;
+    if (k_in % 128 != 0 || hd % 64 != 0 || n_out % 128 != 0) return PKM_ERR_UNSUPPORTED;
+    if (workspace_bytes < kv_matmul_paged_fp8_workspace_size(total_rows, k_in))
+        return PKM_ERR_INVALID_ARG;
+    KvMatmulArgs a{};
+    a.hidden = static_cast<const uint16_t*>(hidden_state);
+    a.row_offsets = input_row_offsets;
+    a.batch = batch;
+    a.total_rows = total_rows;
+    a.k_in = k_in;
+    a.n_out = n_out;
+    a.head_elems = hd;
+    a.cache_layer = static_cast<uint16_t*>(kv_cache->data) +
+                    static_cast<int64_t>(layer_idx) * kv_cache->layer_stride;
+    a.page_stride = kv_cache->page_stride;
+    a.slot_stride = kv_cache->slot_stride;
+    a.kv_stride = kv_cache->kv_stride;
+    a.num_pages = kv_cache->num_pages;
+    a.page_size = kv_cache->page_size;
+    a.max_pages = kv_cache->max_pages_per_seq;
+    a.page_table = kv_cache->page_table;
+    a.cache_lengths = kv_cache->cache_lengths;
+    a.status = dev_status;
+    a.timeout_ns = wait_timeout_ns();
+    a.bn = 128;  // pair tiles of 256 rows x one 128-column weight-scale block
+    a.n_tiles = n_out / 128;
+    a.m_tiles = (total_rows + 255) / 256;
+    a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
+    KvFp8Extra x{};
+    x.q = static_cast<uint8_t*>(workspace);
+    x.q_scale = reinterpret_cast<float*>(
+        static_cast<uint8_t*>(workspace) +
+        align256(static_cast<size_t>(total_rows) * static_cast<size_t>(k_in)));
+    x.w_scale = w_scale;
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
+    alignas(64) CUtensorMap tm_q, tm_w;
+    if (!encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.q, k_in, total_rows,
+                   static_cast<uint64_t>(k_in), 128, 128) ||
+        !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_e4m3, k_in, n_out,
+                   static_cast<uint64_t>(k_in), 128, 64))
+        return PKM_ERR_CUDA;
+    return pkm::launch_kv_matmul_fp8(tm_q, tm_w, a, x, sms, static_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? PKM_OK
                : PKM_ERR_CUDA;

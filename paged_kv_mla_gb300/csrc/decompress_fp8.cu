@@ -196,17 +196,6 @@ constexpr size_t kOffBars = kOffOut + size_t(kEpiWarps) * kOutBufBytes;
 constexpr size_t kSmemBytes = kOffBars + sizeof(Bars) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
 
-// Pair MMA, e4m3 x e4m3 -> fp32 (M = 256 over the two CTAs).
-__device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                              uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decompress_fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_q,
                                const __grid_constant__ CUtensorMap tm_w,

@@ -47,29 +47,6 @@ constexpr size_t kOffBars = kOffOut + size_t(kEpiWarps) * kOutBufBytes;
 constexpr size_t kSmemBytes = kOffBars + sizeof(Bars) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
 
-// Element offset (inside the layer's K plane) of the slot that receives row r, -1 when no
-// request covers r, -2 when the position resolves past the page table or the cache.
-__device__ __forceinline__ int64_t kv_row_dest(const KvMatmulArgs& a, int64_t r) {
-    const uint32_t* iro = a.row_offsets;
-    const int64_t covered = static_cast<int64_t>(__ldg(iro + a.batch));
-    if (r >= a.total_rows || r >= covered) return -1;
-    if (static_cast<uint64_t>(r) < static_cast<uint64_t>(__ldg(iro))) return -1;
-    int lo = 0, hi = a.batch;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (static_cast<uint64_t>(__ldg(iro + mid)) <= static_cast<uint64_t>(r)) lo = mid;
-        else hi = mid;
-    }
-    const uint64_t pos = static_cast<uint64_t>(__ldg(a.cache_lengths + lo)) +
-                         (static_cast<uint64_t>(r) - __ldg(iro + lo));
-    const uint64_t lp = pos / static_cast<uint64_t>(a.page_size);
-    if (lp >= static_cast<uint64_t>(a.max_pages)) return -2;
-    const uint32_t page = __ldg(a.page_table + static_cast<int64_t>(lo) * a.max_pages + lp);
-    if (page >= static_cast<uint32_t>(a.num_pages)) return -2;
-    return static_cast<int64_t>(page) * a.page_stride +
-           static_cast<int64_t>(pos % static_cast<uint64_t>(a.page_size)) * a.slot_stride;
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     kv_matmul_kernel(const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_w, const KvMatmulArgs a) {

@@ -1,0 +1,376 @@
+// kv_matmul_fp8.cu -- the ragged GEMM of kv_matmul_ragged_paged in FP8 with block scales,
+// written into the paged K/V cache.
+//
+// kv_matmul_ragged_paged (Modular MAX, nn/kv_cache_ragged), description and Args: Y =
+// hidden_state x weight on the ragged rows, row i of request b written at cache position
+// cache_lengths[b] + i, columns split K then V.  In FP8 form (the fp8 type and m/n/k scale
+// granularities of mla_prefill_decode_graph_fp8): the bf16 hidden rows are quantised per
+// token per 128 columns (s = amax / 448, q = e4m3_rne(x / s), fp32), the weight is e4m3
+// [n_out, k_in] with fp32 scales per 128 x 128 block, and
+//     Y[r, n] = bf16( sum_kb s_x[r, kb] * s_w[n / 128, kb] * sum_{k in kb} q_x[r, k] q_w[n, k] ).
+//
+// Two kernels:
+//   1. fp8_quantize_rows_kernel: one warp per hidden row quantises it into the workspace
+//      (codes [M, k_in], scales [M, k_in / 128]).
+//   2. kv_matmul_fp8_kernel: clusters of two CTAs over 256 x 128 output tiles (one n tile =
+//      one weight-scale block).  Each CTA streams, per 128-wide k-block, its 128 rows of
+//      quantised A and its 64-row half of the weight block through a 7-stage TMA ring; the
+//      even CTA issues tcgen05.mma.cta_group::2 kind::f8f6f4 (M = 256) into one of four
+//      TMEM accumulators.  Because every k-block carries its own pair of scales, 8 epilogue
+//      warps per CTA fold each k-block's accumulator into fp32 running sums
+//      (acc += s_x * s_w * partial, packed fp32x2 FMAs) and hand it back at once, so the MMAs
+//      of the next k-blocks proceed meanwhile.  After a tile's last k-block the sums are
+//      rounded to bf16 and staged in shared memory; 4 store warps scatter each row's 64-column
+//      segments to its (page, slot) in the K or V plane.
+#include "pkm_device.cuh"
+#include "pkm_internal.h"
+
+namespace pkm {
+namespace {
+
+// ------------------------------------------------------------------------------------
+// 1. quantise the hidden rows
+// ------------------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256)
+    fp8_quantize_rows_kernel(const KvMatmulArgs a, const KvFp8Extra x) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int K = a.k_in;
+    const int chunks = K / 8;  // 16-byte chunks of a row; a 128-column block is 16 of them
+    const int kblocks = K / 128;
+    for (int64_t r = warp_id; r < a.total_rows; r += nwarps) {
+        const uint16_t* src = a.hidden + r * K;
+        uint8_t* qrow = x.q + r * K;
+        for (int base = 0; base < chunks; base += 32) {
+            const int c = base + lane;
+            const bool active = c < chunks;  // a last group of 16 chunks leaves lanes 16-31 idle
+            const uint4 v = active ? ld_nc_v4(src + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+            float f[8];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                f[2 * i] = __uint_as_float(w[i] << 16);
+                f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+            for (int sh = 8; sh >= 1; sh >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
+            const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+            if (!active) continue;
+            const uint32_t lo = e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
+                                (e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
+            const uint32_t hi = e4m3x2(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s)) |
+                                (e4m3x2(__fdiv_rn(f[6], s), __fdiv_rn(f[7], s)) << 16);
+            *reinterpret_cast<uint2*>(qrow + c * 8) = make_uint2(lo, hi);
+            if ((lane & 15) == 0) x.q_scale[r * kblocks + c / 16] = s;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// 2. block-scaled GEMM + scatter
+// ------------------------------------------------------------------------------------
+
+constexpr int kThreads = 448;                  // producer, MMA, 8 epilogue, 4 store warps
+constexpr int kBM = 128;                       // rows per CTA (256 per pair)
+constexpr int kBN = 128;                       // pair N tile = one weight-scale block
+constexpr int kABytes = kBM * 128;             // 128 rows x 128 e4m3
+constexpr int kBBytes = (kBN / 2) * 128;       // this CTA's 64 weight rows x 128 e4m3
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kStages = 7;
+constexpr int kAcc = 4;                        // TMEM accumulators, one per k-block in flight
+constexpr int kEpiWarps = 8;
+constexpr int kStoreWarps = 4;
+constexpr int kFirstStoreWarp = 2 + kEpiWarps;
+constexpr int kOutBufBytes = 32 * 128;
+constexpr uint32_t kTmemCols = kAcc * kBN;
+
+struct Bars {
+    uint64_t full[kStages];     // even CTA: both CTAs' A and B halves of a stage landed
+    uint64_t empty[kStages];    // both CTAs: the pair's MMAs are done with a stage
+    uint64_t t_full[kAcc];      // both CTAs: a k-block's accumulator is ready
+    uint64_t t_empty[kAcc];     // even CTA: both CTAs' epilogues have read it
+    uint64_t st_full;           // the epilogue warps staged a tile's rounded rows
+    uint64_t st_empty;          // the store warps wrote them out
+    struct {
+        int64_t plane_col;      // K/V plane offset + first column inside the head
+        int64_t dst[32];        // per staged row: slot offset in the K plane, -1 = none
+    } box[kEpiWarps];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+constexpr size_t kOffStages = 0;
+constexpr size_t kOffOut = kOffStages + size_t(kStages) * kStageBytes;
+constexpr size_t kOffBars = kOffOut + size_t(kEpiWarps) * kOutBufBytes;
+constexpr size_t kSmemBytes = kOffBars + sizeof(Bars) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    kv_matmul_fp8_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_w, const KvMatmulArgs a,
+                         const KvFp8Extra x) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sStages = smem + kOffStages;
+    uint8_t* sOut = smem + kOffOut;
+    Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int KB = a.k_in / 128;
+    const int64_t T = a.total_tiles;  // pair tiles
+    const int64_t P = gridDim.x / 2;
+    const int64_t pair = blockIdx.x / 2;
+    const int64_t t_begin = T * pair / P;
+    const int64_t t_end = T * (pair + 1) / P;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int i = 0; i < kAcc; ++i) {
+            mbar_init(&bars->t_full[i], 1);
+            mbar_init(&bars->t_empty[i], 2 * kEpiWarps);
+        }
+        mbar_init(&bars->st_full, kEpiWarps);
+        mbar_init(&bars->st_empty, kStoreWarps);
+        mbar_init(&bars->mma_done, 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&bars->tmem_base, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tm_q);
+        tma_prefetch_map(&tm_w);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const WaitCtl wc{&bars->abort_flag, a.status, a.timeout_ns};
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // A rows are re-read for every n tile of their block and the weight by every
+            // block: both are kept in L2 ahead of the scattered cache writes
+            const uint64_t keep = policy_evict_last();
+            RingPos rp;
+            bool issued[kStages] = {};
+            uint32_t last_phase[kStages] = {};
+            bool ok = true;
+            for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid() && ok; w.next()) {
+                const int64_t m = w.m * 2 + rank;  // this CTA's 128-row block
+                const int n = static_cast<int>(w.n);
+                for (int kb = 0; kb < KB; ++kb) {
+                    const uint32_t s = rp.stage, ph = rp.phase;
+                    if (!mbar_wait(&bars->empty[s], ph ^ 1, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = sStages + s * kStageBytes;
+                    const uint32_t full_leader = mapa_shared(smem_u32(&bars->full[s]), 0);
+                    if (leader) mbar_arrive_expect_tx(&bars->full[s], 2u * kStageBytes);
+                    tma_load_2d_pair(st, &tm_q, full_leader, kb * 128,
+                                     static_cast<int32_t>(m * kBM), keep);
+                    tma_load_2d_pair(st + kABytes, &tm_w, full_leader, kb * 128,
+                                     n * kBN + static_cast<int>(rank) * (kBN / 2), keep);
+                    issued[s] = true;
+                    last_phase[s] = ph;
+                    rp.next(kStages);
+                }
+            }
+            if (!ok) {
+                if (leader) {
+                    for (int s = 0; s < kStages; ++s)
+                        if (issued[s]) mbar_wait(&bars->full[s], last_phase[s], wc, false);
+                } else {
+                    spin_ns(50000);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (leader && lane == 0) {
+            const uint32_t idesc = idesc_e4m3(256, kBN);
+            RingPos rp;
+            uint32_t kbg = 0;  // k-blocks issued so far: accumulator kbg % kAcc
+            bool ok = true;
+            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    const uint32_t s = rp.stage, ph = rp.phase;
+                    const uint32_t acc = kbg % kAcc, aph = (kbg / kAcc) & 1;
+                    if (!mbar_wait(&bars->full[s], ph, wc) ||
+                        !mbar_wait(&bars->t_empty[acc], aph ^ 1, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sStages + s * kStageBytes);
+                    const uint32_t b_addr = a_addr + kABytes;
+                    const uint32_t d = tmem + acc * kBN;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_e4m3_pair(d, sdesc_sw128(a_addr + k * 32, 16, 1024),
+                                      sdesc_sw128(b_addr + k * 32, 16, 1024), idesc,
+                                      k != 0 ? 1u : 0u);
+                    mma_commit_pair(&bars->t_full[acc], 3);
+                    mma_commit_pair(&bars->empty[s], 3);
+                    rp.next(kStages);
+                    ++kbg;
+                }
+            }
+            mma_commit_pair(&bars->mma_done, 1);
+            mbar_wait(&bars->mma_done, 0, wc, false);
+        }
+    } else if (warp < kFirstStoreWarp) {
+        // 8 epilogue warps: warp w reads TMEM lane quarter w % 4 (32 rows) and one 64-column
+        // half of the tile, and keeps 64 fp32 running sums across the tile's k-blocks.
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        const uint32_t stage = smem_u32(sOut + (warp - 2) * kOutBufBytes);
+        const uint32_t t_empty_leader = mapa_shared(smem_u32(&bars->t_empty[0]), 0);
+        auto& box = bars->box[warp - 2];
+        uint32_t kbg = 0, tile_i = 0;
+        int64_t cur_m = -1, my_dst = -1, my_row = 0;
+        bool ok = true;
+        for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid() && ok; w.next()) {
+            const int64_t m = w.m * 2 + rank;
+            const int n = static_cast<int>(w.n);
+            if (m != cur_m) {
+                cur_m = m;
+                my_row = m * kBM + q * 32 + lane;
+                my_dst = kv_row_dest(a, my_row);
+                if (my_dst == -2 && h == 0) report(a.status, PKM_ERR_OUT_OF_RANGE);
+            }
+            // scales of this row and n tile, fetched one k-block ahead of their use
+            const float* srow = x.q_scale + my_row * KB;
+            const float* wrow = x.w_scale + static_cast<int64_t>(n) * KB;
+            float sa_next = my_dst >= 0 ? __ldg(srow) : 0.0f;
+            float ws_next = __ldg(wrow);
+            float acc[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+            for (int kb = 0; kb < KB; ++kb) {
+                const float cs = sa_next * ws_next;
+                if (kb + 1 < KB) {
+                    sa_next = my_dst >= 0 ? __ldg(srow + kb + 1) : 0.0f;
+                    ws_next = __ldg(wrow + kb + 1);
+                }
+                const uint32_t slot = kbg % kAcc, ph = (kbg / kAcc) & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars->t_full[slot], ph, wc))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tbase =
+                    tmem + (static_cast<uint32_t>(q * 32) << 16) + slot * kBN + h * 64;
+                // two 32-column halves: 14 warps leave 128 registers a thread
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[32];
+                    tmem_ld_x32(tbase + half * 32, v);
+                    tmem_ld_wait();
+                    if (half == 1) {  // the accumulator has been read: back to the MMAs
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive_remote(t_empty_leader + slot * sizeof(uint64_t));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2)
+                        fma2(acc[half * 32 + j], acc[half * 32 + j + 1], cs,
+                             __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+                }
+                ++kbg;
+            }
+            if (!ok) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->st_empty, (tile_i & 1) ^ 1, wc))) break;
+            const uint32_t rowaddr = stage + lane * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                st_shared_v4(rowaddr + ((j ^ (lane & 7)) << 4),
+                             pack_bf16x2(acc[8 * j], acc[8 * j + 1]),
+                             pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
+                             pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]),
+                             pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
+            box.dst[lane] = my_dst;
+            if (lane == 0) {
+                // 64 output columns of one box lie entirely in the K or the V plane
+                const int col0 = n * kBN + h * 64;
+                box.plane_col = col0 < a.head_elems ? col0 : a.kv_stride + (col0 - a.head_elems);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->st_full);
+            ++tile_i;
+        }
+    } else {
+        // 4 store warps: store warp s writes the boxes of epilogue warps 2s and 2s + 1, each
+        // row's 64 columns as one 128-byte segment at its slot (eight lanes per row).
+        const int s = warp - kFirstStoreWarp;
+        const int chunk = lane & 7;
+        uint32_t tile_i = 0;
+        for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid(); w.next()) {
+            if (!mbar_wait(&bars->st_full, tile_i & 1, wc)) break;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int src = 2 * s + e;
+                const uint32_t bx = smem_u32(sOut + src * kOutBufBytes);
+                const int64_t pc = bars->box[src].plane_col;
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int r = it * 4 + (lane >> 3);
+                    const uint4 v = ld_shared_v4(bx + r * 128 + ((chunk ^ (r & 7)) << 4));
+                    const int64_t d = bars->box[src].dst[r];
+                    if (d >= 0) st_v4(a.cache_layer + pc + d + chunk * 8, v);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->st_empty);
+            ++tile_i;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_kv_matmul_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_w,
+                                 KvMatmulArgs args, KvFp8Extra extra, int num_sms,
+                                 cudaStream_t stream) {
+    int64_t blocks = (static_cast<int64_t>(args.total_rows) + 7) / 8;  // 8 rows per block
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    fp8_quantize_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(args, extra);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kv_matmul_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    const int64_t max_pairs = num_sms / 2;
+    const int64_t pairs = args.total_tiles < max_pairs ? args.total_tiles : max_pairs;
+    kv_matmul_fp8_kernel<<<static_cast<unsigned>(2 * pairs), kThreads, kSmemBytes, stream>>>(
+        tm_q, tm_w, args, extra);
+    return cudaGetLastError();
+}
+
+}  // namespace pkm

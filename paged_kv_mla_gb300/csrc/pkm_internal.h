@@ -90,6 +90,13 @@ struct KvMatmulArgs {
     int64_t total_tiles;
 };
 
+// FP8 kv_matmul operands: the quantised hidden rows (workspace) and the weight scales.
+struct KvFp8Extra {
+    uint8_t* q;                    // [M, k_in] e4m3 (workspace)
+    float* q_scale;                // [M, k_in/128] (workspace)
+    const float* w_scale;          // [n_out/128, k_in/128]
+};
+
 // Launchers (return a CUDA error code; 0 = success).  Tensor maps are encoded by the
 // caller.
 cudaError_t launch_decompress_bf16(const CUtensorMap& tm_w, const CUtensorMap& tm_wv,
@@ -104,6 +111,9 @@ cudaError_t launch_decompress_fp8_gemm(const CUtensorMap& tm_q, const CUtensorMa
                                        Fp8Extra extra, int num_sms, cudaStream_t stream);
 cudaError_t launch_kv_matmul(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                              KvMatmulArgs args, int num_sms, cudaStream_t stream);
+cudaError_t launch_kv_matmul_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_w,
+                                 KvMatmulArgs args, KvFp8Extra extra, int num_sms,
+                                 cudaStream_t stream);
 cudaError_t launch_cache_write(CacheWriteArgs args, int num_sms, cudaStream_t stream);
 cudaError_t launch_wait_timeout_check(int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 
@@ -146,6 +156,31 @@ __device__ __forceinline__ int64_t decompress_row_source(const DecompressArgs& a
 __device__ __forceinline__ int64_t decompress_row_end(const DecompressArgs& a) {
     const int64_t covered = static_cast<int64_t>(__ldg(a.row_offsets + a.batch));
     return covered < a.buffer_length ? covered : a.buffer_length;
+}
+
+// kv_matmul rows: element offset (inside the layer's K plane) of the slot that receives
+// row r, -1 when no request covers r, -2 when the position resolves past the page table or
+// the cache.  Row i of request b (the largest b with row_offsets[b] <= r) is position
+// cache_lengths[b] + i.
+__device__ __forceinline__ int64_t kv_row_dest(const KvMatmulArgs& a, int64_t r) {
+    const uint32_t* iro = a.row_offsets;
+    const int64_t covered = static_cast<int64_t>(__ldg(iro + a.batch));
+    if (r >= a.total_rows || r >= covered) return -1;
+    if (static_cast<uint64_t>(r) < static_cast<uint64_t>(__ldg(iro))) return -1;
+    int lo = 0, hi = a.batch;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<uint64_t>(__ldg(iro + mid)) <= static_cast<uint64_t>(r)) lo = mid;
+        else hi = mid;
+    }
+    const uint64_t pos = static_cast<uint64_t>(__ldg(a.cache_lengths + lo)) +
+                         (static_cast<uint64_t>(r) - __ldg(iro + lo));
+    const uint64_t lp = pos / static_cast<uint64_t>(a.page_size);
+    if (lp >= static_cast<uint64_t>(a.max_pages)) return -2;
+    const uint32_t page = __ldg(a.page_table + static_cast<int64_t>(lo) * a.max_pages + lp);
+    if (page >= static_cast<uint32_t>(a.num_pages)) return -2;
+    return static_cast<int64_t>(page) * a.page_stride +
+           static_cast<int64_t>(pos % static_cast<uint64_t>(a.page_size)) * a.slot_stride;
 }
 
 }  // namespace pkm

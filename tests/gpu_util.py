@@ -144,7 +144,13 @@ class DeviceKvMatmul:
         self.k = k
         self.hidden = dev(k.hidden_state)
         self.iro = dev(k.input_row_offsets)
-        self.weight = dev(k.weight)
+        if k.fp8:
+            self.weight = dev(k.w_e4m3)
+            self.w_scale = dev(k.w_scale)
+            nbytes = pkm.kv_matmul_paged_fp8_workspace_size(k.total_rows, k.k_in)
+            self.workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+        else:
+            self.weight = dev(k.weight)
         self.cache = dev(k.cache)
         self.pt = dev(k.page_table)
         self.cl = dev(k.cache_lengths)
@@ -157,8 +163,22 @@ class DeviceKvMatmul:
 
     def run(self, stream=None, check=True):
         import paged_kv_mla_gb300 as pkm
+        if self.k.fp8:
+            return pkm.kv_matmul_paged_fp8(self.hidden, self.iro, self.weight, self.w_scale, self.pc,
+                                           self.k.layer_idx, self.workspace,
+                                           dev_status=self.status, stream=stream, check=check)
         return pkm.kv_matmul_paged(self.hidden, self.iro, self.weight, self.pc, self.k.layer_idx,
                                    dev_status=self.status, stream=stream, check=check)
+
+    def quantised_rows(self):
+        """(codes [M, k_in], scales [M, k_in/128]) from the FP8 workspace."""
+        torch.cuda.synchronize()
+        M, K = self.k.total_rows, self.k.k_in
+        ws = self.workspace.cpu().numpy()
+        q = ws[:M * K].reshape(M, K)
+        off = (M * K + 255) // 256 * 256
+        s = ws[off:off + M * (K // 128) * 4].view(np.float32).reshape(M, K // 128)
+        return q, s
 
     def results(self):
         torch.cuda.synchronize()

@@ -27,7 +27,7 @@ def main():
     ap.add_argument("--launches", type=int, default=4)
     args = ap.parse_args()
     w = workloads.WORKLOADS[args.workload]()
-    if args.workload == "kv_matmul_write_path":
+    if args.workload.startswith("kv_matmul"):
         g = DeviceKvMatmul(w)
     elif args.workload == "cache_write_path":
         g = DeviceCacheWrite(w)

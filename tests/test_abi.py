@@ -35,6 +35,7 @@ def test_header_declares_the_entry_points():
     for n in ["mla_decompress_k_paged", "mla_decompress_k_paged_fp8", "mla_decompress_kv_paged",
               "mla_decompress_kv_paged_fp8", "mla_cache_write_paged",
               "mla_decompress_k_paged_fp8_qcache", "mla_cache_write_paged_qcache",
+              "kv_matmul_paged_fp8", "kv_matmul_paged_fp8_workspace_size",
               "mla_decompress_k_paged_fp8_workspace_size", "kv_matmul_paged", "pkm_status_string"]:
         assert n in names
 
@@ -155,6 +156,20 @@ def test_invalid_calls_return_status_without_a_gpu(lib):
     assert call_qw(qc(kv_lora_rank=256, slot_stride=272)) == pkm.PKM_ERR_INVALID_ARG  # payload 280
     assert call_qw(qc(kv_lora_rank=192, slot_stride=224)) == pkm.PKM_ERR_UNSUPPORTED  # R % 128
     assert call_qw(qc(cache_lengths=None)) == pkm.PKM_ERR_INVALID_ARG
+    # FP8 kv_matmul
+    assert pkm.kv_matmul_paged_fp8_workspace_size(10, 256) == 2560 + 256   # 2560 codes, 80 B scales
+    assert pkm.kv_matmul_paged_fp8_workspace_size(10, 200) == 0
+    kvc = _cache(pkm, row_elems=128, cache_lengths=co)
+    hid = torch.zeros(4, 256, dtype=torch.int16)
+
+    def call_kf(n_out=256, h=hid, w=None, ws_=wsp):
+        w = torch.zeros(n_out, h.shape[1], dtype=torch.uint8) if w is None else w
+        return pkm.kv_matmul_paged_fp8(h, bro, w, ws, kvc, 0, ws_, stream=0, check=False)
+    assert call_kf(n_out=192) == pkm.PKM_ERR_INVALID_ARG                # not HD or 2 HD
+    assert call_kf(h=torch.zeros(4, 192, dtype=torch.int16)) == pkm.PKM_ERR_UNSUPPORTED  # k_in % 128
+    assert call_kf(ws_=wsp[:100]) == pkm.PKM_ERR_INVALID_ARG            # workspace too small
+    assert call_kf(ws_=wsp[64:]) == pkm.PKM_ERR_INVALID_ARG             # workspace misaligned
+    assert call_kf(h=hid[:0]) == pkm.PKM_OK                             # no rows
 
 
 def test_oracle_and_product_share_no_code():

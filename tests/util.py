@@ -107,5 +107,15 @@ def oracle_cache_write_q(c: CacheWriteInputs):
     return st, view.data.reshape(c.cache.shape)
 
 
+def oracle_kv_matmul_fp8(k: KvMatmulInputs):
+    """Runs the FP8 kv_matmul oracle on a copy of the cache; returns (status, cache_after,
+    q, s)."""
+    view = kv_cache_view(k, data=k.cache.copy())
+    st, q, s = oracle.kv_matmul_fp8(k.hidden_state, k.input_row_offsets, k.batch, k.total_rows,
+                                    k.w_e4m3, k.w_scale, view, k.head_elems, k.cache_lengths,
+                                    k.layer_idx)
+    return st, view.data.reshape(k.cache.shape), q, s
+
+
 def e4m3_decode_table() -> np.ndarray:
     return np.array([oracle.e4m3_to_double(c) for c in range(256)], np.float64)
