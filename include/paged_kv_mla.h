@@ -420,7 +420,9 @@ pkm_status kv_matmul_paged(const void* hidden_state, const uint32_t* input_row_o
  * Bytes of device workspace kv_matmul_paged_fp8 needs for total_rows hidden rows of k_in
  * columns (0 for invalid sizes).  Layout:
  *     offset 0                                e4m3 codes [total_rows, k_in]
- *     offset align256(total_rows * k_in)      fp32 scales [total_rows, k_in / 128]
+ *     offset align256(total_rows * k_in)      fp32 scales [k_in / 128, total_rows]
+ *                                             (k-block-major: scale of row r, block kb at
+ *                                             kb * total_rows + r)
  */
 size_t kv_matmul_paged_fp8_workspace_size(int32_t total_rows, int32_t k_in);
 

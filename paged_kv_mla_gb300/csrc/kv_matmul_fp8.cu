@@ -10,8 +10,9 @@
 //     Y[r, n] = bf16( sum_kb s_x[r, kb] * s_w[n / 128, kb] * sum_{k in kb} q_x[r, k] q_w[n, k] ).
 //
 // Two kernels:
-//   1. fp8_quantize_rows_kernel: one warp per hidden row quantises it into the workspace
-//      (codes [M, k_in], scales [M, k_in / 128]).
+//   1. fp8_quantize_rows_kernel: warps quantise 256-column slices of the hidden rows into the
+//      workspace (codes [M, k_in]; scales k-block-major, [k_in / 128, M], so that the
+//      epilogue's per-k-block scale loads of 32 consecutive rows are one 128-byte line).
 //   2. kv_matmul_fp8_kernel: clusters of two CTAs over 256 x 128 output tiles (one n tile =
 //      one weight-scale block).  Each CTA streams, per 128-wide k-block, its 128 rows of
 //      quantised A and its 64-row half of the weight block through a 7-stage TMA ring; the
@@ -32,23 +33,40 @@ namespace {
 // 1. quantise the hidden rows
 // ------------------------------------------------------------------------------------
 
+// A task is one 256-column slice of one row (two 128-column blocks, one per half-warp: a
+// 16-byte chunk a lane).  Each warp takes four tasks at a time and issues their loads before
+// any arithmetic, so that enough bytes are in flight to keep HBM busy.
+constexpr int kQuantUnroll = 4;
+
 __global__ void __launch_bounds__(256)
     fp8_quantize_rows_kernel(const KvMatmulArgs a, const KvFp8Extra x) {
     const int lane = threadIdx.x & 31;
     const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int K = a.k_in;
-    const int chunks = K / 8;  // 16-byte chunks of a row; a 128-column block is 16 of them
-    const int kblocks = K / 128;
-    for (int64_t r = warp_id; r < a.total_rows; r += nwarps) {
-        const uint16_t* src = a.hidden + r * K;
-        uint8_t* qrow = x.q + r * K;
-        for (int base = 0; base < chunks; base += 32) {
-            const int c = base + lane;
-            const bool active = c < chunks;  // a last group of 16 chunks leaves lanes 16-31 idle
-            const uint4 v = active ? ld_nc_v4(src + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+    const int chunks = K / 8;            // 16-byte chunks of a row
+    const int slices = (chunks + 31) / 32;
+    const int64_t tasks = static_cast<int64_t>(a.total_rows) * slices;
+    for (int64_t t0 = warp_id; t0 < tasks; t0 += kQuantUnroll * nwarps) {
+        uint4 v[kQuantUnroll];
+        int64_t row[kQuantUnroll];
+        int chunk[kQuantUnroll];
+        bool act[kQuantUnroll];
+#pragma unroll
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            const int64_t t = t0 + u * nwarps;
+            row[u] = t / slices;
+            chunk[u] = static_cast<int>(t - row[u] * slices) * 32 + lane;
+            // a last slice of one block leaves lanes 16-31 idle
+            act[u] = t < tasks && chunk[u] < chunks;
+            v[u] = act[u] ? ld_nc_v4(a.hidden + row[u] * K + chunk[u] * 8)
+                          : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            if (t0 + u * nwarps >= tasks) break;  // warp-uniform
             float f[8];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 f[2 * i] = __uint_as_float(w[i] << 16);
@@ -61,13 +79,14 @@ __global__ void __launch_bounds__(256)
             for (int sh = 8; sh >= 1; sh >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
             const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-            if (!active) continue;
+            if (!act[u]) continue;
             const uint32_t lo = e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
                                 (e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
             const uint32_t hi = e4m3x2(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s)) |
                                 (e4m3x2(__fdiv_rn(f[6], s), __fdiv_rn(f[7], s)) << 16);
-            *reinterpret_cast<uint2*>(qrow + c * 8) = make_uint2(lo, hi);
-            if ((lane & 15) == 0) x.q_scale[r * kblocks + c / 16] = s;
+            *reinterpret_cast<uint2*>(x.q + row[u] * K + chunk[u] * 8) = make_uint2(lo, hi);
+            if ((lane & 15) == 0)
+                x.q_scale[static_cast<int64_t>(chunk[u] / 16) * a.total_rows + row[u]] = s;
         }
     }
 }
@@ -256,19 +275,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 my_dst = kv_row_dest(a, my_row);
                 if (my_dst == -2 && h == 0) report(a.status, PKM_ERR_OUT_OF_RANGE);
             }
-            // scales of this row and n tile, fetched one k-block ahead of their use
-            const float* srow = x.q_scale + my_row * KB;
+            // scales of this row and n tile, fetched two k-blocks ahead of their use (the row
+            // scales of a k-block are contiguous over rows: one line per warp)
+            const float* scol = x.q_scale + my_row;
+            const int64_t sstep = a.total_rows;
             const float* wrow = x.w_scale + static_cast<int64_t>(n) * KB;
-            float sa_next = my_dst >= 0 ? __ldg(srow) : 0.0f;
-            float ws_next = __ldg(wrow);
+            const bool live = my_dst >= 0;
+            float sa0 = live ? __ldg(scol) : 0.0f, ws0 = __ldg(wrow);
+            float sa1 = (live && KB > 1) ? __ldg(scol + sstep) : 0.0f;
+            float ws1 = KB > 1 ? __ldg(wrow + 1) : 0.0f;
             float acc[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
             for (int kb = 0; kb < KB; ++kb) {
-                const float cs = sa_next * ws_next;
-                if (kb + 1 < KB) {
-                    sa_next = my_dst >= 0 ? __ldg(srow + kb + 1) : 0.0f;
-                    ws_next = __ldg(wrow + kb + 1);
+                const float cs = sa0 * ws0;
+                sa0 = sa1;
+                ws0 = ws1;
+                if (kb + 2 < KB) {
+                    sa1 = live ? __ldg(scol + (kb + 2) * sstep) : 0.0f;
+                    ws1 = __ldg(wrow + kb + 2);
                 }
                 const uint32_t slot = kbg % kAcc, ph = (kbg / kAcc) & 1;
                 if (!__all_sync(0xffffffffu, mbar_wait(&bars->t_full[slot], ph, wc))) {
@@ -356,7 +381,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 cudaError_t launch_kv_matmul_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_w,
                                  KvMatmulArgs args, KvFp8Extra extra, int num_sms,
                                  cudaStream_t stream) {
-    int64_t blocks = (static_cast<int64_t>(args.total_rows) + 7) / 8;  // 8 rows per block
+    const int64_t tasks = static_cast<int64_t>(args.total_rows) * ((args.k_in / 8 + 31) / 32);
+    int64_t blocks = (tasks + 8 * kQuantUnroll - 1) / (8 * kQuantUnroll);  // 8 warps a block
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;

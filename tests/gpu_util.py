@@ -171,13 +171,14 @@ class DeviceKvMatmul:
                                    dev_status=self.status, stream=stream, check=check)
 
     def quantised_rows(self):
-        """(codes [M, k_in], scales [M, k_in/128]) from the FP8 workspace."""
+        """(codes [M, k_in], scales [M, k_in/128]) from the FP8 workspace (which holds the
+        scales k-block-major)."""
         torch.cuda.synchronize()
         M, K = self.k.total_rows, self.k.k_in
         ws = self.workspace.cpu().numpy()
         q = ws[:M * K].reshape(M, K)
         off = (M * K + 255) // 256 * 256
-        s = ws[off:off + M * (K // 128) * 4].view(np.float32).reshape(M, K // 128)
+        s = ws[off:off + M * (K // 128) * 4].view(np.float32).reshape(K // 128, M).T.copy()
         return q, s
 
     def results(self):
