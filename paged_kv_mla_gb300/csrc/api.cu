@@ -735,8 +735,8 @@ pkm_status kv_matmul_paged_fp8(const void* hidden_state, const uint32_t* input_r
     a.cache_lengths = kv_cache->cache_lengths;
     a.status = dev_status;
     a.timeout_ns = wait_timeout_ns();
-    a.bn = 128;  // pair tiles of 256 rows x one 128-column weight-scale block
-    a.n_tiles = n_out / 128;
+    a.bn = 256;  // pair tiles of 256 rows x two 128-column weight-scale blocks
+    a.n_tiles = (n_out + 255) / 256;  // an odd number of blocks leaves a half tile
     a.m_tiles = (total_rows + 255) / 256;
     a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
     KvFp8Extra x{};
@@ -751,7 +751,7 @@ pkm_status kv_matmul_paged_fp8(const void* hidden_state, const uint32_t* input_r
     if (!encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.q, k_in, total_rows,
                    static_cast<uint64_t>(k_in), 128, 128) ||
         !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_e4m3, k_in, n_out,
-                   static_cast<uint64_t>(k_in), 128, 64))
+                   static_cast<uint64_t>(k_in), 128, 128))
         return PKM_ERR_CUDA;
     return pkm::launch_kv_matmul_fp8(tm_q, tm_w, a, x, sms, static_cast<cudaStream_t>(stream)) ==
                    cudaSuccess

@@ -13,16 +13,17 @@
 //   1. fp8_quantize_rows_kernel: warps quantise 256-column slices of the hidden rows into the
 //      workspace (codes [M, k_in]; scales k-block-major, [k_in / 128, M], so that the
 //      epilogue's per-k-block scale loads of 32 consecutive rows are one 128-byte line).
-//   2. kv_matmul_fp8_kernel: clusters of two CTAs over 256 x 128 output tiles (one n tile =
-//      one weight-scale block).  Each CTA streams, per 128-wide k-block, its 128 rows of
-//      quantised A and its 64-row half of the weight block through a 7-stage TMA ring; the
-//      even CTA issues tcgen05.mma.cta_group::2 kind::f8f6f4 (M = 256) into one of four
-//      TMEM accumulators.  Because every k-block carries its own pair of scales, 8 epilogue
-//      warps per CTA fold each k-block's accumulator into fp32 running sums
-//      (acc += s_x * s_w * partial, packed fp32x2 FMAs) and hand it back at once, so the MMAs
-//      of the next k-blocks proceed meanwhile.  After a tile's last k-block the sums are
-//      rounded to bf16 and staged in shared memory; 4 store warps scatter each row's 64-column
-//      segments to its (page, slot) in the K or V plane.
+//   2. kv_matmul_fp8_kernel: clusters of two CTAs over 256 x 256 output tiles (two
+//      weight-scale blocks; N = 256 keeps the e4m3 MMAs at full rate, where N = 128 ran at
+//      about half).  Each CTA streams, per 128-wide k-block, its 128 rows of quantised A and
+//      its 128-row half of the weight through a 5-stage TMA ring; the even CTA issues
+//      tcgen05.mma.cta_group::2 kind::f8f6f4 (M = 256) into one of two 256-column TMEM
+//      accumulators.  Because every k-block carries its own scales, 16 epilogue warps per
+//      CTA (32 rows x 64 columns each) fold each k-block's accumulator into fp32 running sums
+//      (acc += s_x * s_w * partial, packed fp32x2 FMAs) and hand it back at once, so the
+//      MMAs of the next k-block proceed meanwhile.  After a tile's last k-block each warp
+//      rounds its sums to bf16 and scatters its rows' 64-column segments to their
+//      (page, slot) in the K or V plane through a swizzled shared-memory box.
 #include "pkm_device.cuh"
 #include "pkm_internal.h"
 
@@ -95,18 +96,16 @@ __global__ void __launch_bounds__(256)
 // 2. block-scaled GEMM + scatter
 // ------------------------------------------------------------------------------------
 
-constexpr int kThreads = 448;                  // producer, MMA, 8 epilogue, 4 store warps
+constexpr int kEpiWarps = 16;
+constexpr int kThreads = 32 * (2 + kEpiWarps);  // producer, MMA, 16 epilogue warps
 constexpr int kBM = 128;                       // rows per CTA (256 per pair)
-constexpr int kBN = 128;                       // pair N tile = one weight-scale block
+constexpr int kBN = 256;                       // pair N tile: two weight-scale blocks
 constexpr int kABytes = kBM * 128;             // 128 rows x 128 e4m3
-constexpr int kBBytes = (kBN / 2) * 128;       // this CTA's 64 weight rows x 128 e4m3
+constexpr int kBBytes = (kBN / 2) * 128;       // this CTA's 128 weight rows x 128 e4m3
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kStages = 7;
-constexpr int kAcc = 4;                        // TMEM accumulators, one per k-block in flight
-constexpr int kEpiWarps = 8;
-constexpr int kStoreWarps = 4;
-constexpr int kFirstStoreWarp = 2 + kEpiWarps;
-constexpr int kOutBufBytes = 32 * 128;
+constexpr int kStages = 5;
+constexpr int kAcc = 2;                        // TMEM accumulators of 256 columns
+constexpr int kOutBufBytes = 32 * 128;         // a warp's 32 x 64 bf16 box
 constexpr uint32_t kTmemCols = kAcc * kBN;
 
 struct Bars {
@@ -114,12 +113,6 @@ struct Bars {
     uint64_t empty[kStages];    // both CTAs: the pair's MMAs are done with a stage
     uint64_t t_full[kAcc];      // both CTAs: a k-block's accumulator is ready
     uint64_t t_empty[kAcc];     // even CTA: both CTAs' epilogues have read it
-    uint64_t st_full;           // the epilogue warps staged a tile's rounded rows
-    uint64_t st_empty;          // the store warps wrote them out
-    struct {
-        int64_t plane_col;      // K/V plane offset + first column inside the head
-        int64_t dst[32];        // per staged row: slot offset in the K plane, -1 = none
-    } box[kEpiWarps];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -147,6 +140,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
     const int KB = a.k_in / 128;
+    const int NB = a.n_out / 128;     // weight-scale blocks along n
     const int64_t T = a.total_tiles;  // pair tiles
     const int64_t P = gridDim.x / 2;
     const int64_t pair = blockIdx.x / 2;
@@ -162,8 +156,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(&bars->t_full[i], 1);
             mbar_init(&bars->t_empty[i], 2 * kEpiWarps);
         }
-        mbar_init(&bars->st_full, kEpiWarps);
-        mbar_init(&bars->st_empty, kStoreWarps);
         mbar_init(&bars->mma_done, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -206,6 +198,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (leader) mbar_arrive_expect_tx(&bars->full[s], 2u * kStageBytes);
                     tma_load_2d_pair(st, &tm_q, full_leader, kb * 128,
                                      static_cast<int32_t>(m * kBM), keep);
+                    // weight rows past n_out (a half tile at the end) load as zeros
                     tma_load_2d_pair(st + kABytes, &tm_w, full_leader, kb * 128,
                                      n * kBN + static_cast<int>(rank) * (kBN / 2), keep);
                     issued[s] = true;
@@ -255,15 +248,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mma_commit_pair(&bars->mma_done, 1);
             mbar_wait(&bars->mma_done, 0, wc, false);
         }
-    } else if (warp < kFirstStoreWarp) {
-        // 8 epilogue warps: warp w reads TMEM lane quarter w % 4 (32 rows) and one 64-column
-        // half of the tile, and keeps 64 fp32 running sums across the tile's k-blocks.
+    } else {
+        // 16 epilogue warps: warp w reads TMEM lane quarter w % 4 (32 rows) and one 64-column
+        // quarter of the tile, keeps 64 fp32 running sums across the tile's k-blocks, and at
+        // the end of the tile rounds them and scatters its rows' 64-column segments.
+        const int e = warp - 2;
         const int q = warp & 3;
-        const int h = (warp - 2) >> 2;
-        const uint32_t stage = smem_u32(sOut + (warp - 2) * kOutBufBytes);
+        const int cq = e >> 2;                  // column quarter 0..3
+        const uint32_t stage = smem_u32(sOut + e * kOutBufBytes);
         const uint32_t t_empty_leader = mapa_shared(smem_u32(&bars->t_empty[0]), 0);
-        auto& box = bars->box[warp - 2];
-        uint32_t kbg = 0, tile_i = 0;
+        uint32_t kbg = 0;
         int64_t cur_m = -1, my_dst = -1, my_row = 0;
         bool ok = true;
         for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid() && ok; w.next()) {
@@ -273,14 +267,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 cur_m = m;
                 my_row = m * kBM + q * 32 + lane;
                 my_dst = kv_row_dest(a, my_row);
-                if (my_dst == -2 && h == 0) report(a.status, PKM_ERR_OUT_OF_RANGE);
+                if (my_dst == -2 && cq == 0) report(a.status, PKM_ERR_OUT_OF_RANGE);
             }
-            // scales of this row and n tile, fetched two k-blocks ahead of their use (the row
-            // scales of a k-block are contiguous over rows: one line per warp)
+            const int nb = n * 2 + (cq >> 1);   // weight-scale block of these columns
+            const bool cols_live = nb < NB;     // false in the empty half of a last half tile
+            // scales of this row and column block, fetched two k-blocks ahead of their use
+            // (the row scales of a k-block are contiguous over rows: one line per warp)
             const float* scol = x.q_scale + my_row;
             const int64_t sstep = a.total_rows;
-            const float* wrow = x.w_scale + static_cast<int64_t>(n) * KB;
-            const bool live = my_dst >= 0;
+            const float* wrow = x.w_scale + static_cast<int64_t>(cols_live ? nb : 0) * KB;
+            const bool live = my_dst >= 0 && cols_live;
             float sa0 = live ? __ldg(scol) : 0.0f, ws0 = __ldg(wrow);
             float sa1 = (live && KB > 1) ? __ldg(scol + sstep) : 0.0f;
             float ws1 = KB > 1 ? __ldg(wrow + 1) : 0.0f;
@@ -302,28 +298,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t tbase =
-                    tmem + (static_cast<uint32_t>(q * 32) << 16) + slot * kBN + h * 64;
-                // two 32-column halves: 14 warps leave 128 registers a thread
+                    tmem + (static_cast<uint32_t>(q * 32) << 16) + slot * kBN + cq * 64;
+                // four 16-column quarters: 18 warps leave under 100 registers a thread
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t v[32];
-                    tmem_ld_x32(tbase + half * 32, v);
+                for (int part = 0; part < 4; ++part) {
+                    uint32_t v[16];
+                    tmem_ld_x16(tbase + part * 16, v);
                     tmem_ld_wait();
-                    if (half == 1) {  // the accumulator has been read: back to the MMAs
+                    if (part == 3) {  // the accumulator has been read: back to the MMAs
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0)
                             mbar_arrive_remote(t_empty_leader + slot * sizeof(uint64_t));
                     }
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2)
-                        fma2(acc[half * 32 + j], acc[half * 32 + j + 1], cs,
+                    for (int j = 0; j < 16; j += 2)
+                        fma2(acc[part * 16 + j], acc[part * 16 + j + 1], cs,
                              __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
                 }
                 ++kbg;
             }
-            if (!ok) break;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars->st_empty, (tile_i & 1) ^ 1, wc))) break;
+            if (!ok || !cols_live) continue;
+            // round, stage the 32 x 64 box (swizzled 128-byte rows), scatter each row's
+            // segment to its slot, eight lanes a row; 64 columns lie in one K or V plane
             const uint32_t rowaddr = stage + lane * 128;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -332,40 +329,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                              pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
                              pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]),
                              pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
-            box.dst[lane] = my_dst;
-            if (lane == 0) {
-                // 64 output columns of one box lie entirely in the K or the V plane
-                const int col0 = n * kBN + h * 64;
-                box.plane_col = col0 < a.head_elems ? col0 : a.kv_stride + (col0 - a.head_elems);
+            __syncwarp();
+            const int col0 = n * kBN + cq * 64;
+            const int64_t pc = col0 < a.head_elems ? col0 : a.kv_stride + (col0 - a.head_elems);
+            const int chunk = lane & 7;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int r = it * 4 + (lane >> 3);
+                const int64_t d = __shfl_sync(0xffffffffu, my_dst, r);
+                const uint4 v = ld_shared_v4(stage + r * 128 + ((chunk ^ (r & 7)) << 4));
+                if (d >= 0) st_v4(a.cache_layer + pc + d + chunk * 8, v);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->st_full);
-            ++tile_i;
-        }
-    } else {
-        // 4 store warps: store warp s writes the boxes of epilogue warps 2s and 2s + 1, each
-        // row's 64 columns as one 128-byte segment at its slot (eight lanes per row).
-        const int s = warp - kFirstStoreWarp;
-        const int chunk = lane & 7;
-        uint32_t tile_i = 0;
-        for (TileWalk w(t_begin, t_end, a.n_tiles); w.valid(); w.next()) {
-            if (!mbar_wait(&bars->st_full, tile_i & 1, wc)) break;
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int src = 2 * s + e;
-                const uint32_t bx = smem_u32(sOut + src * kOutBufBytes);
-                const int64_t pc = bars->box[src].plane_col;
-#pragma unroll
-                for (int it = 0; it < 8; ++it) {
-                    const int r = it * 4 + (lane >> 3);
-                    const uint4 v = ld_shared_v4(bx + r * 128 + ((chunk ^ (r & 7)) << 4));
-                    const int64_t d = bars->box[src].dst[r];
-                    if (d >= 0) st_v4(a.cache_layer + pc + d + chunk * 8, v);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->st_empty);
-            ++tile_i;
         }
     }
 
