@@ -34,38 +34,33 @@ namespace {
 // 1. quantise the hidden rows
 // ------------------------------------------------------------------------------------
 
-// A task is one 256-column slice of one row (two 128-column blocks, one per half-warp: a
-// 16-byte chunk a lane).  Each warp takes four tasks at a time and issues their loads before
-// any arithmetic, so that enough bytes are in flight to keep HBM busy.
+// Grid: blockIdx.y = a 256-column slice of the rows (two 128-column blocks, one per
+// half-warp, a 16-byte chunk a lane), blockIdx.x and the warp pick rows.  Each warp takes
+// four rows at a time and issues their loads before any arithmetic, so that enough bytes
+// are in flight to keep HBM busy.
 constexpr int kQuantUnroll = 4;
 
 __global__ void __launch_bounds__(256)
     fp8_quantize_rows_kernel(const KvMatmulArgs a, const KvFp8Extra x) {
     const int lane = threadIdx.x & 31;
-    const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t warp_x = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t nwarps_x = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     const int K = a.k_in;
-    const int chunks = K / 8;            // 16-byte chunks of a row
-    const int slices = (chunks + 31) / 32;
-    const int64_t tasks = static_cast<int64_t>(a.total_rows) * slices;
-    for (int64_t t0 = warp_id; t0 < tasks; t0 += kQuantUnroll * nwarps) {
+    const int chunk = static_cast<int>(blockIdx.y) * 32 + lane;  // this lane's 16-byte chunk
+    const bool act = chunk < K / 8;  // a last slice of one block leaves lanes 16-31 idle
+    const int64_t M = a.total_rows;
+    for (int64_t r0 = warp_x; r0 < M; r0 += kQuantUnroll * nwarps_x) {
         uint4 v[kQuantUnroll];
-        int64_t row[kQuantUnroll];
-        int chunk[kQuantUnroll];
-        bool act[kQuantUnroll];
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
-            const int64_t t = t0 + u * nwarps;
-            row[u] = t / slices;
-            chunk[u] = static_cast<int>(t - row[u] * slices) * 32 + lane;
-            // a last slice of one block leaves lanes 16-31 idle
-            act[u] = t < tasks && chunk[u] < chunks;
-            v[u] = act[u] ? ld_nc_v4(a.hidden + row[u] * K + chunk[u] * 8)
-                          : make_uint4(0u, 0u, 0u, 0u);
+            const int64_t r = r0 + u * nwarps_x;
+            v[u] = (act && r < M) ? ld_nc_v4(a.hidden + r * K + chunk * 8)
+                                  : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
-            if (t0 + u * nwarps >= tasks) break;  // warp-uniform
+            const int64_t r = r0 + u * nwarps_x;
+            if (r >= M) break;  // warp-uniform
             float f[8];
             const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
@@ -80,14 +75,13 @@ __global__ void __launch_bounds__(256)
             for (int sh = 8; sh >= 1; sh >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
             const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-            if (!act[u]) continue;
+            if (!act) continue;
             const uint32_t lo = e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
                                 (e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
             const uint32_t hi = e4m3x2(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s)) |
                                 (e4m3x2(__fdiv_rn(f[6], s), __fdiv_rn(f[7], s)) << 16);
-            *reinterpret_cast<uint2*>(x.q + row[u] * K + chunk[u] * 8) = make_uint2(lo, hi);
-            if ((lane & 15) == 0)
-                x.q_scale[static_cast<int64_t>(chunk[u] / 16) * a.total_rows + row[u]] = s;
+            *reinterpret_cast<uint2*>(x.q + r * K + chunk * 8) = make_uint2(lo, hi);
+            if ((lane & 15) == 0) x.q_scale[static_cast<int64_t>(chunk / 16) * M + r] = s;
         }
     }
 }
@@ -356,12 +350,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 cudaError_t launch_kv_matmul_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_w,
                                  KvMatmulArgs args, KvFp8Extra extra, int num_sms,
                                  cudaStream_t stream) {
-    const int64_t tasks = static_cast<int64_t>(args.total_rows) * ((args.k_in / 8 + 31) / 32);
-    int64_t blocks = (tasks + 8 * kQuantUnroll - 1) / (8 * kQuantUnroll);  // 8 warps a block
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    fp8_quantize_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(args, extra);
+    const int slices = (args.k_in / 8 + 31) / 32;
+    int64_t bx = (static_cast<int64_t>(args.total_rows) + 8 * kQuantUnroll - 1) / (8 * kQuantUnroll);
+    const int64_t cap = (static_cast<int64_t>(num_sms) * 8 + slices - 1) / slices;  // 8 blocks an SM
+    if (bx > cap) bx = cap;
+    if (bx < 1) bx = 1;
+    fp8_quantize_rows_kernel<<<dim3(static_cast<unsigned>(bx), static_cast<unsigned>(slices)), 256,
+                               0, stream>>>(args, extra);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kv_matmul_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -12,7 +12,7 @@ import torch
 import oracle
 import workloads
 from gpu_util import FP8_TOL, DeviceKvMatmul, assert_close_bf16
-from util import kv_cache_view, oracle_kv_matmul_fp8
+from util import e4m3_midpoint_bf16_values, kv_cache_view, oracle_kv_matmul_fp8
 
 pytestmark = pytest.mark.gpu
 
@@ -101,3 +101,22 @@ def test_kv_matmul_fp8_write_path_full_size():
     st, ref, _, _ = oracle_kv_matmul_fp8(sub)
     changed_ref = ref != k.cache
     assert_close_bf16(out[changed_ref], ref[changed_ref], FP8_TOL, "fp8 kv cache values")
+
+
+def test_kv_matmul_fp8_quantisation_at_e4m3_midpoints_bit_exact():
+    """Hidden blocks with a power-of-two scale (amax = 448 * 2^k) whose other values sit on
+    e4m3 rounding midpoints or one bf16 step beside them (normal and subnormal e4m3 range):
+    the quantised rows must equal the oracle's bit for bit."""
+    k = workloads.make_kv_matmul("kvmid", 641, [40, 25], [0, 3], 512, 1, 128, 16, fp8=True)
+    vals = bf16_bits = e4m3_midpoint_bf16_values()
+    rng = np.random.default_rng(641)
+    h = np.empty_like(k.hidden_state)
+    for r in range(h.shape[0]):
+        for kb in range(4):
+            j = int(rng.integers(-4, 3))
+            blk = workloads.bf16_bits_to_float(rng.choice(bf16_bits, 128)).astype(np.float64)
+            blk *= np.where(rng.random(128) < 0.5, -1.0, 1.0) * 2.0 ** j
+            blk[int(rng.integers(0, 128))] = 448.0 * 2.0 ** j
+            h[r, kb * 128:(kb + 1) * 128] = [oracle.double_to_bf16(v) for v in blk]
+    k.hidden_state = h
+    check_full(k)

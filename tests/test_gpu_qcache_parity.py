@@ -16,7 +16,8 @@ import torch
 import oracle
 import workloads
 from gpu_util import FP8_TOL, DeviceCacheWrite, DeviceDecompress, assert_close_bf16
-from util import oracle_cache_write_q, oracle_decompress_qcache, qcache_view
+from util import (e4m3_midpoint_bf16_values, oracle_cache_write_q, oracle_decompress_qcache,
+                  qcache_view)
 
 pytestmark = pytest.mark.gpu
 SQ = workloads.SENTINEL_QBYTE
@@ -210,28 +211,12 @@ def test_qcache_write_full_size():
         assert np.array_equal(outq[k][R:R + 2 * P].view(np.uint16), outb[k][R:])
 
 
-def _midpoint_values():
-    """e4m3 rounding midpoints (normal and subnormal range) and their bf16 neighbours, as
-    multiples of the block scale."""
-    mids = [(1 + (2 * j + 1) / 16) * 2.0 ** e for e in range(-6, 9) for j in range(8)
-            if (1 + (2 * j + 1) / 16) * 2.0 ** e < 448]
-    mids += [(2 * i + 1) * 2.0 ** -10 for i in range(7)]
-    bits = [workloads.bf16_bits_to_float(np.array([oracle.double_to_bf16(m)], np.uint16))[0]
-            for m in mids]
-    assert all(float(b) == m for b, m in zip(bits, mids))
-    out = []
-    for m in mids:
-        h = oracle.double_to_bf16(m)
-        out += [h, h + 1, h - 1]          # the midpoint and one bf16 step either side
-    return np.array(out, np.uint16)
-
-
 def test_fp8_quantisation_at_e4m3_midpoints_bit_exact():
     """Blocks whose scale is a power of two (amax = 448 * 2^k) and whose other values sit on
     e4m3 rounding midpoints (ties to even) or one bf16 step beside them, in the normal and
     subnormal e4m3 range: the GPU's codes and scales must equal the oracle's bit for bit."""
     d = workloads.make_decompress("mid", 951, [64, 64], [0, 0], 16, 512, 64, 128, fp8=True)
-    vals = _midpoint_values()
+    vals = e4m3_midpoint_bf16_values()
     rng = np.random.default_rng(951)
     cache = d.cache.copy()
     L, Pg, S, C = cache.shape
@@ -262,7 +247,7 @@ def test_qcache_write_at_e4m3_midpoints_bit_exact():
     keep the rope exact: the quantised slots must equal the oracle's bit for bit."""
     c = workloads.make_cache_write("cwmid", 953, [70, 33], [0, 5], 512, 64, 16, quantised=True)
     rng = np.random.default_rng(953)
-    vals = workloads.bf16_bits_to_float(_midpoint_values()).astype(np.float64)
+    vals = workloads.bf16_bits_to_float(e4m3_midpoint_bf16_values()).astype(np.float64)
     vals = vals[vals * 8 < 448] / 8
     gamma = rng.choice(vals, 512)
     gamma[::128] = 56.0

@@ -5,7 +5,7 @@ from __future__ import annotations
 import numpy as np
 
 import oracle
-from workloads import CacheWriteInputs, DecompressInputs, KvMatmulInputs
+from workloads import CacheWriteInputs, DecompressInputs, KvMatmulInputs, bf16_bits_to_float
 
 
 def f32_to_bf16_exact(a) -> np.ndarray:
@@ -119,3 +119,19 @@ def oracle_kv_matmul_fp8(k: KvMatmulInputs):
 
 def e4m3_decode_table() -> np.ndarray:
     return np.array([oracle.e4m3_to_double(c) for c in range(256)], np.float64)
+
+
+def e4m3_midpoint_bf16_values():
+    """e4m3 rounding midpoints (normal and subnormal range) and their bf16 neighbours, as
+    multiples of the block scale."""
+    mids = [(1 + (2 * j + 1) / 16) * 2.0 ** e for e in range(-6, 9) for j in range(8)
+            if (1 + (2 * j + 1) / 16) * 2.0 ** e < 448]
+    mids += [(2 * i + 1) * 2.0 ** -10 for i in range(7)]
+    bits = [bf16_bits_to_float(np.array([oracle.double_to_bf16(m)], np.uint16))[0]
+            for m in mids]
+    assert all(float(b) == m for b, m in zip(bits, mids))
+    out = []
+    for m in mids:
+        h = oracle.double_to_bf16(m)
+        out += [h, h + 1, h - 1]          # the midpoint and one bf16 step either side
+    return np.array(out, np.uint16)
