@@ -1,22 +1,28 @@
 /*
  * paged_kv_mla.h -- C ABI of the GB300 (sm_103a) paged-KV MLA hot path.
  *
- * Three operations, after the Modular MAX kernel pages that define them:
+ The operations, after the Modular MAX kernel pages that define them:
  *
  *   mla_decompress_k_paged      generic_flare_mla_decompress_k_cache_ragged_paged
  *                               (nn/kv_cache_ragged; signature, description and Args):
  *                               gather each request's latent K rows out of a paged cache
  *                               into k_latent_buffer, then k_buffer = latent[:, :R] . W_k^T.
+ *   mla_decompress_kv_paged     the same gather feeding the K and the V (w_uv) up-projection.
  *   mla_decompress_k_paged_fp8  the same decompress as the K-decompress stage of
  *                               mla_prefill_decode_graph_fp8 (attention/gpu/mla_graph;
  *                               Parameters m/n/k_scale_granularity, Args w_k, w_k_scale,
  *                               buffer_row_offsets, cache_offsets, buffer_length), with an
  *                               e4m3 W_k carrying 128x128 fp32 block scales and the latent
- *                               quantised per token per 128-column block.
- *   kv_matmul_paged             kv_matmul_ragged_paged (nn/kv_cache_ragged; description and
+ *                               quantised per token per 128-column block
+ *                               (+ _kv_ with w_uv / w_uv_scale, + _noalloc).
+ *   mla_decompress_k_paged_fp8_qcache  the FP8 decompress reading a quantised paged cache.
+ *   mla_cache_write_paged[_qcache]     the cache-write side of mla_prefill_decode_graph_fp8
+ *                               (kv_norm_gamma, epsilon, freqs_cis): RMSNorm and RoPE of new
+ *                               latent rows stored into a bf16 or a quantised paged cache.
+ *   kv_matmul_paged[_fp8]       kv_matmul_ragged_paged (nn/kv_cache_ragged; description and
  *                               Args): Y = hidden_state . weight on the ragged rows, with
  *                               row i of request b written into the paged K/V cache at
- *                               position cache_lengths[b] + i.
+ *                               position cache_lengths[b] + i (bf16, or FP8 block-scaled).
  *
  * Conventions shared by every entry point
  *   - Every tensor argument is DEVICE memory on the current CUDA device, allocated and
