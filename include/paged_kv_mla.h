@@ -1,7 +1,7 @@
 /*
  * paged_kv_mla.h -- C ABI of the GB300 (sm_103a) paged-KV MLA hot path.
  *
- The operations, after the Modular MAX kernel pages that define them:
+ * The operations, after the Modular MAX kernel pages that define them:
  *
  *   mla_decompress_k_paged      generic_flare_mla_decompress_k_cache_ragged_paged
  *                               (nn/kv_cache_ragged; signature, description and Args):
