@@ -10,7 +10,7 @@
 //     Y[r, n] = bf16( sum_kb s_x[r, kb] * s_w[n / 128, kb] * sum_{k in kb} q_x[r, k] q_w[n, k] ).
 //
 // Two kernels:
-//   1. fp8_quantize_rows_kernel: warps quantise 256-column slices of the hidden rows into the
+//   1. fp8_quantize_rows_kernel: warps quantise 512-column slices of the hidden rows into the
 //      workspace (codes [M, k_in]; scales k-block-major, [k_in / 128, M], so that the
 //      epilogue's per-k-block scale loads of 32 consecutive rows are one 128-byte line).
 //   2. kv_matmul_fp8_kernel: clusters of two CTAs over 256 x 256 output tiles (two
@@ -34,8 +34,8 @@ namespace {
 // 1. quantise the hidden rows
 // ------------------------------------------------------------------------------------
 
-// Grid: blockIdx.y = a 256-column slice of the rows (two 128-column blocks, one per
-// half-warp, a 16-byte chunk a lane), blockIdx.x and the warp pick rows.  Each warp takes
+// Grid: blockIdx.y = a 512-column slice of the rows (four 128-column blocks, eight lanes a
+// block, 16 values = 32 bytes a lane), blockIdx.x and the warp pick rows.  Each warp takes
 // four rows at a time and issues their loads before any arithmetic, so that enough bytes
 // are in flight to keep HBM busy.
 constexpr int kQuantUnroll = 4;
@@ -46,42 +46,45 @@ __global__ void __launch_bounds__(256)
     const int64_t warp_x = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nwarps_x = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     const int K = a.k_in;
-    const int chunk = static_cast<int>(blockIdx.y) * 32 + lane;  // this lane's 16-byte chunk
-    const bool act = chunk < K / 8;  // a last slice of one block leaves lanes 16-31 idle
+    const int col = static_cast<int>(blockIdx.y) * 512 + lane * 16;  // this lane's 16 columns
+    const bool act = col < K;  // a last slice of fewer blocks leaves whole 8-lane groups idle
     const int64_t M = a.total_rows;
     for (int64_t r0 = warp_x; r0 < M; r0 += kQuantUnroll * nwarps_x) {
-        uint4 v[kQuantUnroll];
+        uint4 v[kQuantUnroll][2];
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
             const int64_t r = r0 + u * nwarps_x;
-            v[u] = (act && r < M) ? ld_nc_v4(a.hidden + r * K + chunk * 8)
-                                  : make_uint4(0u, 0u, 0u, 0u);
+            const bool ld = act && r < M;
+            const uint16_t* src = a.hidden + r * K + col;
+            v[u][0] = ld ? ld_nc_v4(src) : make_uint4(0u, 0u, 0u, 0u);
+            v[u][1] = ld ? ld_nc_v4(src + 8) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
             const int64_t r = r0 + u * nwarps_x;
             if (r >= M) break;  // warp-uniform
-            float f[8];
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                f[2 * i] = __uint_as_float(w[i] << 16);
-                f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-            }
+            float f[16];
+            const uint32_t w[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
+                                   v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
             float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+            for (int i = 0; i < 8; ++i) {
+                f[2 * i] = __uint_as_float(w[i] << 16);
+                f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+            }
 #pragma unroll
-            for (int sh = 8; sh >= 1; sh >>= 1)
+            for (int sh = 4; sh >= 1; sh >>= 1)  // the eight lanes of one block
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
             const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
             if (!act) continue;
-            const uint32_t lo = e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
-                                (e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
-            const uint32_t hi = e4m3x2(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s)) |
-                                (e4m3x2(__fdiv_rn(f[6], s), __fdiv_rn(f[7], s)) << 16);
-            *reinterpret_cast<uint2*>(x.q + r * K + chunk * 8) = make_uint2(lo, hi);
-            if ((lane & 15) == 0) x.q_scale[static_cast<int64_t>(chunk / 16) * M + r] = s;
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                o[i] = e4m3x2(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s)) |
+                       (e4m3x2(__fdiv_rn(f[4 * i + 2], s), __fdiv_rn(f[4 * i + 3], s)) << 16);
+            st_v4(x.q + r * K + col, make_uint4(o[0], o[1], o[2], o[3]));
+            if ((lane & 7) == 0) x.q_scale[static_cast<int64_t>(col / 128) * M + r] = s;
         }
     }
 }
@@ -350,7 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 cudaError_t launch_kv_matmul_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_w,
                                  KvMatmulArgs args, KvFp8Extra extra, int num_sms,
                                  cudaStream_t stream) {
-    const int slices = (args.k_in / 8 + 31) / 32;
+    const int slices = (args.k_in + 511) / 512;
     int64_t bx = (static_cast<int64_t>(args.total_rows) + 8 * kQuantUnroll - 1) / (8 * kQuantUnroll);
     const int64_t cap = (static_cast<int64_t>(num_sms) * 8 + slices - 1) / slices;  // 8 blocks an SM
     if (bx > cap) bx = cap;
