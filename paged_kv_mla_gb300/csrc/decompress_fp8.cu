@@ -7,11 +7,11 @@
 // m = 1, n = k = 128.
 //
 // Two kernels:
-//   1. fp8_gather_quantize_kernel: one warp per output row resolves the row through the
-//      page table, copies the bf16 latent row to k_latent_buffer with 16-byte vector
-//      loads/stores, and quantises its first kv_lora_rank columns per 128-column block
-//      (s = amax / 448, q = e4m3_rne_satfinite(x / s), fp32) into the workspace.  Every
-//      row is quantised exactly once, however many n tiles later consume it.
+//   1. fp8_gather_quantize_kernel: one warp per output row (two rows in flight) resolves the
+//      row through the page table, copies the bf16 latent row to k_latent_buffer with
+//      16-byte vector loads/stores, and quantises its first kv_lora_rank columns per
+//      128-column block (s = amax / 448, q = e4m3_rne_satfinite(x / s), fp32) into the
+//      workspace.  Every row is quantised exactly once, however many n tiles consume it.
 //   2. decompress_fp8_gemm_kernel: clusters of two CTAs (a CTA pair) over 256 x 128 output
 //      tiles (one n tile = one weight-scale block; with w_uv the V tiles follow the K tiles
 //      and reuse the same quantised rows).  Each CTA brings its 128 rows of the
@@ -37,6 +37,12 @@ namespace {
 // 1. gather + quantise
 // ------------------------------------------------------------------------------------
 
+// One warp per output row, two rows at a time: the rows are resolved and all their loads
+// issued before any arithmetic.  A lane holds 16 nope values (32 bytes), so a 128-column
+// block is eight lanes (kv_lora_rank <= 512 fits one pass); lanes below rope_dim / 8 also
+// carry one 16-byte chunk of the rope columns.
+constexpr int kGatherRows = 2;
+
 __global__ void __launch_bounds__(256)
     fp8_gather_quantize_kernel(const DecompressArgs a, const Fp8Extra x) {
     const int lane = threadIdx.x & 31;
@@ -45,49 +51,58 @@ __global__ void __launch_bounds__(256)
     const int64_t row_end = decompress_row_end(a);
     const int R = a.kv_lora_rank;
     const int C = a.latent_cols;
-    const int nope_chunks = R / 8;
-    const int all_chunks = C / 8;
     const int kblocks = R / 128;
-    for (int64_t r = warp_id; r < row_end; r += nwarps) {
-        const int64_t off = decompress_row_source(a, r, row_end);
-        if (off < 0) {
-            if (off == -2 && lane == 0) report(a.status, PKM_ERR_OUT_OF_RANGE);
-            continue;
-        }
-        const uint16_t* src = a.cache_layer + off;
-        uint16_t* lat = a.k_latent + r * C;
-        uint8_t* qrow = x.q_latent + r * R;
-        for (int base = 0; base < nope_chunks; base += 32) {
-            const int c = base + lane;
-            const bool active = c < nope_chunks;
-            const uint4 v = active ? ld_nc_v4(src + c * 8) : make_uint4(0u, 0u, 0u, 0u);
-            if (active) st_v4(lat + c * 8, v);
-            float f[8];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const bool nope = lane * 16 < R;
+    const bool rope = lane < (C - R) / 8;
+    for (int64_t r0 = warp_id; r0 < row_end; r0 += kGatherRows * nwarps) {
+        int64_t off[kGatherRows];
+        uint4 nv[kGatherRows][2], rv[kGatherRows];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                f[2 * i] = __uint_as_float(w[i] << 16);
-                f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        for (int u = 0; u < kGatherRows; ++u) {
+            const int64_t r = r0 + u * nwarps;
+            off[u] = decompress_row_source(a, r, row_end);  // -1 past row_end too
+            const uint16_t* src = a.cache_layer + (off[u] >= 0 ? off[u] : 0);
+            const bool live = off[u] >= 0;
+            nv[u][0] = live && nope ? ld_nc_v4(src + lane * 16) : make_uint4(0u, 0u, 0u, 0u);
+            nv[u][1] = live && nope ? ld_nc_v4(src + lane * 16 + 8) : make_uint4(0u, 0u, 0u, 0u);
+            rv[u] = live && rope ? ld_nc_v4(src + R + lane * 8) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kGatherRows; ++u) {
+            if (off[u] < 0) {  // warp-uniform
+                if (off[u] == -2 && lane == 0) report(a.status, PKM_ERR_OUT_OF_RANGE);
+                continue;
             }
+            const int64_t r = r0 + u * nwarps;
+            uint16_t* lat = a.k_latent + r * C;
+            if (nope) {
+                st_v4(lat + lane * 16, nv[u][0]);
+                st_v4(lat + lane * 16 + 8, nv[u][1]);
+            }
+            if (rope) st_v4(lat + R + lane * 8, rv[u]);
+            float f[16];
+            const uint32_t w[8] = {nv[u][0].x, nv[u][0].y, nv[u][0].z, nv[u][0].w,
+                                   nv[u][1].x, nv[u][1].y, nv[u][1].z, nv[u][1].w};
             float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-            // one 128-column block = 16 chunks = one half-warp
+            for (int i = 0; i < 8; ++i) {
+                f[2 * i] = __uint_as_float(w[i] << 16);
+                f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+            }
 #pragma unroll
-            for (int sh = 8; sh >= 1; sh >>= 1)
+            for (int sh = 4; sh >= 1; sh >>= 1)  // the eight lanes of one block
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
             const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-            if (active) {
-                uint32_t lo = e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
-                              (e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
-                uint32_t hi = e4m3x2(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s)) |
-                              (e4m3x2(__fdiv_rn(f[6], s), __fdiv_rn(f[7], s)) << 16);
-                *reinterpret_cast<uint2*>(qrow + c * 8) = make_uint2(lo, hi);
-                if ((lane & 15) == 0) x.q_scale[r * kblocks + c / 16] = s;
-            }
+            if (!nope) continue;
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                o[i] = e4m3x2(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s)) |
+                       (e4m3x2(__fdiv_rn(f[4 * i + 2], s), __fdiv_rn(f[4 * i + 3], s)) << 16);
+            st_v4(x.q_latent + r * R + lane * 16, make_uint4(o[0], o[1], o[2], o[3]));
+            if ((lane & 7) == 0) x.q_scale[r * kblocks + lane / 8] = s;
         }
-        for (int c = nope_chunks + lane; c < all_chunks; c += 32)
-            st_v4(lat + c * 8, ld_nc_v4(src + c * 8));
     }
 }
 
@@ -481,7 +496,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 cudaError_t launch_fp8_gather_quantize(DecompressArgs args, Fp8Extra extra, int num_sms,
                                        cudaStream_t stream) {
     const int64_t rows = args.buffer_length;
-    int64_t blocks = (rows + 7) / 8;  // 8 warps (rows in flight) per block
+    int64_t blocks = (rows + 8 * kGatherRows - 1) / (8 * kGatherRows);  // 8 warps per block
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
