@@ -45,6 +45,7 @@ constexpr int kGatherRows = 2;
 
 __global__ void __launch_bounds__(256)
     fp8_gather_quantize_kernel(const DecompressArgs a, const Fp8Extra x) {
+    griddep_launch_dependents();  // the GEMM may start its prologue; it waits for our writes
     const int lane = threadIdx.x & 31;
     const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -120,6 +121,7 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint32_t two, float& lo, float& hi
 
 __global__ void __launch_bounds__(256)
     fp8_gather_qcache_kernel(const DecompressArgs a, const Fp8Extra x) {
+    griddep_launch_dependents();  // the GEMM may start its prologue; it waits for our writes
     const int lane = threadIdx.x & 31;
     const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -263,6 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncthreads();
     cluster_sync_all();
     tc_fence_after();
+    griddep_wait();  // the prepass's quantised rows (this kernel is its programmatic dependent)
     const uint32_t tmem = bars->tmem_base;
     const WaitCtl wc{&bars->abort_flag, a.status, a.timeout_ns};
     const int64_t row_end = decompress_row_end(a);
@@ -524,9 +527,8 @@ cudaError_t launch_decompress_fp8_gemm(const CUtensorMap& tm_q, const CUtensorMa
     if (e != cudaSuccess) return e;
     const int64_t max_pairs = num_sms / 2;
     const int64_t pairs = args.total_tiles < max_pairs ? args.total_tiles : max_pairs;
-    decompress_fp8_gemm_kernel<<<static_cast<unsigned>(2 * pairs), kThreads, kSmemBytes, stream>>>(
-        tm_q, tm_w, tm_wv, args, extra);
-    return cudaGetLastError();
+    return launch_dependent(decompress_fp8_gemm_kernel, static_cast<unsigned>(2 * pairs), kThreads,
+                            kSmemBytes, stream, tm_q, tm_w, tm_wv, args, extra);
 }
 
 }  // namespace pkm

@@ -42,6 +42,7 @@ constexpr int kQuantUnroll = 4;
 
 __global__ void __launch_bounds__(256)
     fp8_quantize_rows_kernel(const KvMatmulArgs a, const KvFp8Extra x) {
+    griddep_launch_dependents();  // the GEMM may start its prologue; it waits for our writes
     const int lane = threadIdx.x & 31;
     const int64_t warp_x = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nwarps_x = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -169,6 +170,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncthreads();
     cluster_sync_all();
     tc_fence_after();
+    griddep_wait();  // the prepass's quantised rows (this kernel is its programmatic dependent)
     const uint32_t tmem = bars->tmem_base;
     const WaitCtl wc{&bars->abort_flag, a.status, a.timeout_ns};
 
@@ -367,9 +369,8 @@ cudaError_t launch_kv_matmul_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_
     if (e != cudaSuccess) return e;
     const int64_t max_pairs = num_sms / 2;
     const int64_t pairs = args.total_tiles < max_pairs ? args.total_tiles : max_pairs;
-    kv_matmul_fp8_kernel<<<static_cast<unsigned>(2 * pairs), kThreads, kSmemBytes, stream>>>(
-        tm_q, tm_w, args, extra);
-    return cudaGetLastError();
+    return launch_dependent(kv_matmul_fp8_kernel, static_cast<unsigned>(2 * pairs), kThreads,
+                            kSmemBytes, stream, tm_q, tm_w, args, extra);
 }
 
 }  // namespace pkm

@@ -34,6 +34,21 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
 }
 
 // ------------------------------------------------------------------------------------
+// programmatic dependent launch: a prepass lets the kernel that consumes its output start
+// its prologue early; the consumer waits for the prepass's writes before reading them
+// ------------------------------------------------------------------------------------
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Blocks until every prerequisite grid has completed and its memory operations are visible
+// (returns at once when the kernel was not launched as a dependent).
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ------------------------------------------------------------------------------------
 // mbarrier
 // ------------------------------------------------------------------------------------
 

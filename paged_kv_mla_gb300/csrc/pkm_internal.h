@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 namespace pkm {
 
@@ -96,6 +97,25 @@ struct KvFp8Extra {
     float* q_scale;                // [M, k_in/128] (workspace)
     const float* w_scale;          // [n_out/128, k_in/128]
 };
+
+// Launches `kernel` as a programmatic dependent of the work before it on `stream`: it may
+// start while the previous kernel (a prepass that triggers its dependents) still runs, and
+// waits for that kernel's writes with griddepcontrol.wait before reading them.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                             size_t smem, cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Launchers (return a CUDA error code; 0 = success).  Tensor maps are encoded by the
 // caller.
