@@ -51,6 +51,7 @@ KERNEL_SOURCES = {
     "fp8_gather_quantize_kernel": ["decompress_fp8.cu"],
     "kv_matmul_kernel": ["kv_matmul.cu"],
     "cache_write_kernel": ["cache_write.cu"],
+    "cache_write_q_kernel": ["cache_write.cu"],   # the quantising instantiation
     "fp8_gather_qcache_kernel": ["decompress_fp8.cu"],
     "kv_matmul_fp8_kernel": ["kv_matmul_fp8.cu"],
 }
@@ -360,7 +361,8 @@ def run_ours(args, rank, world, local_rank):
             "workload": cw.name, "rows": cw.total_rows, "ms": tc * 1e3,
             "rows_per_s": cw.total_rows / tc, "gbs": cw.bytes_moved / tc / 1e9,
             "hbm_frac_of_measured": cw.bytes_moved / tc / 1e9 / peaks["hbm_gbs"],
-            "traffic": profiled_traffic("cache_write_kernel") if key == "cache_write" else None,
+            "traffic": profiled_traffic("cache_write_kernel" if key == "cache_write"
+                                        else "cache_write_q_kernel"),
             "launches_per_step": 1}
         del gc, cw
     # FP8 decompress from a quantised cache (codes and scales gathered as they are)

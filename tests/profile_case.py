@@ -29,7 +29,7 @@ def main():
     w = workloads.WORKLOADS[args.workload]()
     if args.workload.startswith("kv_matmul"):
         g = DeviceKvMatmul(w)
-    elif args.workload == "cache_write_path":
+    elif args.workload.startswith("cache_write"):
         g = DeviceCacheWrite(w)
     else:
         g = DeviceDecompress(w, fp8=w.w_k_e4m3 is not None)
