@@ -139,8 +139,8 @@ typedef struct {
 /*
  * bf16 latent-K decompress.
  * Source: generic_flare_mla_decompress_k_cache_ragged_paged -- signature, description
- * ("gathers ... into k_latent_buffer using buffer_row_offsets and cache_offsets, then
- * multiplies by the ... weight"), Args buffer_row_offsets_1d, cache_offsets_1d,
+ * (latent K rows gathered into k_latent_buffer as buffer_row_offsets and cache_offsets
+ * direct, then multiplied by the weight), Args buffer_row_offsets_1d, cache_offsets_1d,
  * buffer_length, weight, kv_collection, layer_idx, k_latent_buffer, k_buffer.
  *
  * For every request b < batch and i < buffer_row_offsets[b+1] - buffer_row_offsets[b]:
@@ -177,8 +177,8 @@ pkm_status mla_decompress_k_paged(const pkm_paged_cache* cache, uint32_t layer_i
 /*
  * bf16 latent-K and V decompress: one gather for both up-projections.
  * Source: generic_flare_mla_decompress_k_cache_ragged_paged (the gather and K, as for
- * mla_decompress_k_paged) and mla_prefill_decode_graph_fp8 -- Args w_uv ("Weight tensor
- * for projecting latent values to V. Shape: [num_heads, v_head_dim, kv_latent_dim]").
+ * mla_decompress_k_paged) and mla_prefill_decode_graph_fp8 -- Args w_uv (the weight that
+ * maps latent rows to V, [num_heads, v_head_dim, kv_latent_dim]).
  *
  * Computes exactly what mla_decompress_k_paged computes (k_latent_buffer, k_buffer) and,
  * for every written row r, head h and d < v_head_dim:
@@ -214,7 +214,7 @@ size_t mla_decompress_k_paged_fp8_workspace_size(int32_t buffer_length, int32_t 
  * FP8 block-scaled latent-K decompress.
  * Source: mla_prefill_decode_graph_fp8 -- Parameters fp8_dtype, fp8_scale_dtype,
  * m_scale_granularity, n_scale_granularity, k_scale_granularity; Args buffer_row_offsets,
- * cache_offsets, buffer_length, w_k ("up-projecting the latent cache to full K",
+ * cache_offsets, buffer_length, w_k (lifts the latent cache to the full K,
  * [num_heads * qk_nope_head_dim, kv_latent_dim]) and w_k_scale.  Granularities are fixed
  * at m = 1, n = 128, k = 128.
  *
@@ -247,9 +247,8 @@ pkm_status mla_decompress_k_paged_fp8(const pkm_paged_cache* cache, uint32_t lay
 /*
  * FP8 block-scaled latent-K and V decompress: one gather and one activation quantisation
  * for both up-projections.
- * Source: mla_prefill_decode_graph_fp8 -- Args w_k, w_k_scale, w_uv ("Weight tensor for
- * projecting latent values to V", [num_heads, v_head_dim, kv_latent_dim]), w_uv_scale
- * ("Scale tensor for w_uv").
+ * Source: mla_prefill_decode_graph_fp8 -- Args w_k, w_k_scale, w_uv (latent-to-V weight,
+ * [num_heads, v_head_dim, kv_latent_dim]), w_uv_scale (its scales; no shape is given).
  *
  * Computes exactly what mla_decompress_k_paged_fp8 computes (k_latent_buffer, k_buffer,
  * the workspace) and, with the same quantised row q[r, :] and scales s[r, kb]:
@@ -279,12 +278,11 @@ pkm_status mla_decompress_kv_paged_fp8(const pkm_paged_cache* cache, uint32_t la
 /*
  * The cache-write side of MLA: new latent rows are RMS-normalised and rotated, then
  * stored into the paged latent cache.
- * Source: mla_prefill_decode_graph_fp8 -- Args kv_input_fn ("load the KV latent values",
- * [tot_seq_len, cache_head_dim]), kv_norm_gamma ("RMSNorm gamma weights for normalizing
- * the KV cache", [kv_lora_rank]), epsilon ("Small constant for numerical stability in
- * RMSNorm"), freqs_cis ("Precomputed RoPE frequency values for rotary position
- * embeddings", [max_seq_len, qk_rope_head_dim]), input_row_offsets, kv_collection,
- * layer_idx.
+ * Source: mla_prefill_decode_graph_fp8 -- Args kv_input_fn (supplies the new latent rows,
+ * [tot_seq_len, cache_head_dim]), kv_norm_gamma (the RMSNorm scale vector applied before
+ * caching, [kv_lora_rank]), epsilon (the RMSNorm stabilising term), freqs_cis (rotary
+ * factors per position, [max_seq_len, qk_rope_head_dim]), input_row_offsets,
+ * kv_collection, layer_idx.
  *
  * For every request b and i < input_row_offsets[b+1] - input_row_offsets[b], with
  * r = input_row_offsets[b] + i (r < total_rows) and position pos = cache_lengths[b] + i:
@@ -396,10 +394,10 @@ pkm_status mla_decompress_k_paged_fp8_noalloc(const pkm_paged_cache* cache, uint
 
 /*
  * Ragged GEMM written into the paged K/V cache.
- * Source: kv_matmul_ragged_paged -- description ("performs a matmul, writing the output
- * into" the KV cache collection) and Args hidden_state (sum(seq_lens), num_heads *
- * head_size), input_row_offsets (batch_size + 1), weight (num_heads * head_size,
- * num_kv_heads * head_size), kv_collection (keys and values), layer_idx.
+ * Source: kv_matmul_ragged_paged -- description (a matmul whose output lands in the KV
+ * cache collection) and Args hidden_state (sum(seq_lens), num_heads * head_size),
+ * input_row_offsets (batch_size + 1), weight (num_heads * head_size,
+ * num_kv_heads * head_size), kv_collection (the K and V cache), layer_idx.
  *
  * For every request b < batch and i < input_row_offsets[b+1] - input_row_offsets[b]:
  *     r = input_row_offsets[b] + i              (skipped when r >= total_rows)

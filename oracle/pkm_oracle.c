@@ -393,8 +393,7 @@ int oracle_decompress_k_fp8_row(const uint16_t* cache, int64_t layer_stride,
 /* ------------------------------------------------------------------------------------ */
 
 /*
- * w_uv is the "weight tensor for projecting latent values to V", shape [num_heads,
- * v_head_dim, kv_latent_dim].  For every written row r (the rows step 1 of the
+ * w_uv maps latent rows to V, shape [num_heads, v_head_dim, kv_latent_dim].  For every written row r (the rows step 1 of the
  * decompress gathered), head h and d < v_head_dim:
  *   v[r, h, d] = bf16_rne( sum_{k < R} latent[r, k] * w_uv[h, d, k] ),
  * summed in fp64 in order of k, over the first R = kv_lora_rank latent columns (the
@@ -559,11 +558,11 @@ int oracle_decompress_kv_fp8_row(const uint16_t* cache, int64_t layer_stride,
 /* ------------------------------------------------------------------------------------ */
 
 /*
- * The graph's Args: kv_input_fn loads "the KV latent values", shape [tot_seq_len,
- * cache_head_dim]; kv_norm_gamma holds "RMSNorm gamma weights for normalizing the KV
- * cache", [kv_lora_rank]; epsilon is the RMSNorm constant; freqs_cis holds "precomputed
- * RoPE frequency values", [max_seq_len, qk_rope_head_dim]; input_row_offsets delimits
- * each request's rows; kv_collection / layer_idx name the cache.
+ * The graph's Args: kv_input_fn supplies the new latent rows, shape [tot_seq_len,
+ * cache_head_dim]; kv_norm_gamma is the RMSNorm scale vector, [kv_lora_rank]; epsilon is
+ * the RMSNorm constant; freqs_cis holds the rotary factors of each position,
+ * [max_seq_len, qk_rope_head_dim]; input_row_offsets delimits each request's rows;
+ * kv_collection / layer_idx name the cache.
  *
  * Readings of the silent points:
  *   - row r = iro[b] + i of the new latent values is token position pos = cache_lengths[b]

@@ -2,10 +2,9 @@
 // rotated, then stored into the paged latent cache.
 //
 // mla_prefill_decode_graph_fp8 (Modular MAX, attention/gpu/mla_graph), Args kv_input_fn
-// (the new "KV latent values", [tot_seq_len, cache_head_dim]), kv_norm_gamma ("RMSNorm
-// gamma weights for normalizing the KV cache", [kv_lora_rank]), epsilon, freqs_cis
-// ("Precomputed RoPE frequency values", [max_seq_len, qk_rope_head_dim]), input_row_offsets,
-// kv_collection and layer_idx.  Row i of request b is token position cache_lengths[b] + i
+// (the new latent rows, [tot_seq_len, cache_head_dim]), kv_norm_gamma (the RMSNorm scale
+// vector, [kv_lora_rank]), epsilon, freqs_cis (rotary factors per position, [max_seq_len,
+// qk_rope_head_dim]), input_row_offsets, kv_collection and layer_idx.  Row i of request b is token position cache_lengths[b] + i
 // (the position kv_matmul_ragged_paged gives new tokens); its first R columns become
 // x_k * gamma_k / sqrt(mean_k x_k^2 + epsilon), its last P columns are rotated pair by pair
 // by the (cos, sin) pairs of freqs_cis[position], and the row is stored, rounded to bf16,
