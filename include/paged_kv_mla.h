@@ -474,6 +474,13 @@ pkm_status pkm_check_wait_timeout(int32_t* dev_status, uint32_t timeout_ms, void
 /* Static, human-readable name of a status code. */
 const char* pkm_status_string(pkm_status status);
 
+/* The cause of the last PKM_ERR_CUDA an entry point returned on the calling thread: the
+ * CUDA runtime's text for the failed call (a launch, an attribute, a device query), or a
+ * note that a tensor map was rejected.  A static string owned by the library, valid until
+ * the thread's next failing call; "no CUDA failure recorded" before any.  Not a part of the
+ * pages' interface: a diagnostic of this library. */
+const char* pkm_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

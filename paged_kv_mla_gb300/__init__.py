@@ -40,7 +40,10 @@ PKM_ERR_TIMEOUT = 5
 class PkmError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {status_string(code)} ({code})")
+        msg = f"{where}: {status_string(code)} ({code})"
+        if code == PKM_ERR_CUDA:
+            msg += f": {last_cuda_error()}"
+        super().__init__(msg)
 
 
 class _CCache(ctypes.Structure):
@@ -64,6 +67,8 @@ class _CQuantCache(ctypes.Structure):
 _vp, _i32, _u32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_size_t
 _lib.pkm_status_string.argtypes = [ctypes.c_int]
 _lib.pkm_status_string.restype = ctypes.c_char_p
+_lib.pkm_last_cuda_error.argtypes = []
+_lib.pkm_last_cuda_error.restype = ctypes.c_char_p
 _lib.mla_decompress_k_paged.argtypes = [ctypes.POINTER(_CCache), _u32, _vp, _vp, _i32, _i32, _i32,
                                         _i32, _vp, _i32, _vp, _vp, _vp, _vp]
 _lib.mla_decompress_k_paged.restype = ctypes.c_int
@@ -109,6 +114,11 @@ _lib.pkm_check_wait_timeout.restype = ctypes.c_int
 
 def status_string(code: int) -> str:
     return _lib.pkm_status_string(int(code)).decode()
+
+
+def last_cuda_error() -> str:
+    """What lies behind the last PKM_ERR_CUDA the library returned on this thread."""
+    return _lib.pkm_last_cuda_error().decode()
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:

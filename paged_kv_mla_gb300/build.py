@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpaged_kv_mla.so")
 SOURCES = ["api.cu", "decompress_bf16.cu", "decompress_fp8.cu", "kv_matmul.cu", "selftest.cu",
-           "decompress_fp8_noalloc.cu", "cache_write.cu", "kv_matmul_fp8.cu"]
+           "decompress_fp8_noalloc.cu", "cache_write.cu", "kv_matmul_fp8.cu",
+           "decompress_fp8_wide.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -191,9 +191,25 @@ DecompressArgs make_decompress_args(const pkm_paged_cache* cache, uint32_t layer
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
+// What lies behind the last PKM_ERR_CUDA this thread returned (pkm_last_cuda_error).
+thread_local const char* g_last_cuda_error = "no CUDA failure recorded";
+
+pkm_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return PKM_OK;
+    g_last_cuda_error = cudaGetErrorString(e);
+    return PKM_ERR_CUDA;
+}
+
+pkm_status encode_failed() {
+    g_last_cuda_error = "cuTensorMapEncodeTiled rejected a tensor map";
+    return PKM_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
+
+const char* pkm_last_cuda_error(void) { return g_last_cuda_error; }
 
 const char* pkm_status_string(pkm_status status) {
     switch (status) {
@@ -264,7 +280,7 @@ pkm_status decompress_bf16(const pkm_paged_cache* cache, uint32_t layer_idx,
         a.n_tiles += nv / bn;
     }
     int sms = 0;
-    if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
+    if (const cudaError_t e = current_sm_count(&sms)) return cuda_status(e);
     a.m_tiles = (buffer_length + 255) / 256;
     a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
     alignas(64) CUtensorMap tm_w;
@@ -272,11 +288,11 @@ pkm_status decompress_bf16(const pkm_paged_cache* cache, uint32_t layer_idx,
     alignas(64) CUtensorMap tm_c = {};
     if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_k, kv_lora_rank, n_out,
                    static_cast<uint64_t>(kv_lora_rank) * 2, 64, bn / 2))
-        return PKM_ERR_CUDA;
+        return encode_failed();
     if (nv > 0) {
         if (!encode_2d(&tm_wv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v.w_uv, kv_lora_rank, nv,
                        static_cast<uint64_t>(kv_lora_rank) * 2, 64, bn / 2))
-            return PKM_ERR_CUDA;
+            return encode_failed();
     } else {
         tm_wv = tm_w;
     }
@@ -286,11 +302,9 @@ pkm_status decompress_bf16(const pkm_paged_cache* cache, uint32_t layer_idx,
     if (a.gather_tma &&
         !encode_cache_gather(&tm_c, a.cache_layer, cache->page_size, cache->num_pages,
                              kv_lora_rank / 64, cache->slot_stride, cache->page_stride))
-        return PKM_ERR_CUDA;
-    return pkm::launch_decompress_bf16(tm_w, tm_wv, tm_c, a, sms,
-                                       static_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? PKM_OK
-               : PKM_ERR_CUDA;
+        return encode_failed();
+    return cuda_status(pkm::launch_decompress_bf16(tm_w, tm_wv, tm_c, a, sms,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 // Body of the FP8 entry points: K alone (v.w_uv == nullptr) or K and V, the activations
@@ -345,6 +359,10 @@ pkm_status decompress_fp8(const pkm_paged_cache* cache, uint32_t layer_idx,
     if (workspace_bytes < mla_decompress_k_paged_fp8_workspace_size(buffer_length, kv_lora_rank))
         return PKM_ERR_INVALID_ARG;
     const int32_t nv = v.w_uv != nullptr ? v.n_v : 0;
+    // 256-wide pair tiles (full-rate e4m3 MMAs) when every projection splits into them,
+    // else 128-wide ones
+    const bool wide = n_out % 256 == 0 && nv % 256 == 0;
+    const int bn = wide ? 256 : 128;
     DecompressArgs a{};
     if (qcache != nullptr) {
         // the same problem over byte strides: the page walk is unit-agnostic
@@ -358,23 +376,24 @@ pkm_status decompress_fp8(const pkm_paged_cache* cache, uint32_t layer_idx,
         view.max_pages_per_seq = qcache->max_pages_per_seq;
         a = make_decompress_args(&view, 0, buffer_row_offsets, cache_offsets, batch,
                                  buffer_length, kv_lora_rank, rope_dim, n_out, k_latent_buffer,
-                                 k_buffer, dev_status, 128);
+                                 k_buffer, dev_status, bn);
         a.cache_layer = nullptr;
         a.qcache_layer = static_cast<const uint8_t*>(qcache->data) +
                          static_cast<int64_t>(layer_idx) * qcache->layer_stride;
     } else {
         a = make_decompress_args(cache, layer_idx, buffer_row_offsets, cache_offsets, batch,
                                  buffer_length, kv_lora_rank, rope_dim, n_out, k_latent_buffer,
-                                 k_buffer, dev_status, 128);
+                                 k_buffer, dev_status, bn);
     }
     a.n_tiles_k = a.n_tiles;
     if (nv > 0) {
         a.v_buffer = static_cast<uint16_t*>(v.v_buffer);
         a.n_out_v = nv;
-        a.n_tiles += nv / 128;
+        a.n_tiles += nv / bn;
     }
     a.m_tiles = (buffer_length + 255) / 256;  // CTA-pair tiles of 256 rows
     a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
+    if (wide && a.total_tiles > INT32_MAX) return PKM_ERR_UNSUPPORTED;  // 32-bit tile walk
     Fp8Extra x{};
     x.q_latent = static_cast<uint8_t*>(workspace);
     x.q_scale = reinterpret_cast<float*>(
@@ -383,29 +402,55 @@ pkm_status decompress_fp8(const pkm_paged_cache* cache, uint32_t layer_idx,
     x.w_scale = w_k_scale;
     x.w_scale_v = nv > 0 ? v.w_uv_scale : nullptr;
     int sms = 0;
-    if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
+    if (const cudaError_t e = current_sm_count(&sms)) return cuda_status(e);
     alignas(64) CUtensorMap tm_q, tm_w, tm_wv;
     if (!encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.q_latent, kv_lora_rank, buffer_length,
-                   static_cast<uint64_t>(kv_lora_rank), 128, 128) ||
-        !encode_kblocks_3d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_k_e4m3, 128, n_out,
+                   static_cast<uint64_t>(kv_lora_rank), 128, 128))
+        return encode_failed();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (wide) {
+        // weights by 128 x 128 boxes (one k-block of a CTA's half tile); outputs viewed as
+        // {64 columns, rows, column blocks of 64} and stored by {64, 128, 4} boxes (a CTA's
+        // 128 rows x 256 columns of one tile)
+        alignas(64) CUtensorMap tm_ok, tm_ov;
+        if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_k_e4m3, kv_lora_rank, n_out,
+                       static_cast<uint64_t>(kv_lora_rank), 128, 128) ||
+            !encode_kblocks_3d(&tm_ok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_buffer, 64,
+                               buffer_length, n_out / 64, static_cast<uint64_t>(n_out) * 2, 128,
+                               128, 4))
+            return encode_failed();
+        if (nv > 0) {
+            if (!encode_2d(&tm_wv, CU_TENSOR_MAP_DATA_TYPE_UINT8, v.w_uv, kv_lora_rank, nv,
+                           static_cast<uint64_t>(kv_lora_rank), 128, 128) ||
+                !encode_kblocks_3d(&tm_ov, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v.v_buffer, 64,
+                                   buffer_length, nv / 64, static_cast<uint64_t>(nv) * 2, 128,
+                                   128, 4))
+                return encode_failed();
+        } else {
+            tm_wv = tm_w;
+            tm_ov = tm_ok;
+        }
+        const cudaError_t ge = qcache != nullptr ? pkm::launch_fp8_gather_qcache(a, x, sms, s)
+                                                 : pkm::launch_fp8_gather_quantize(a, x, sms, s);
+        if (ge != cudaSuccess) return cuda_status(ge);
+        return cuda_status(pkm::launch_decompress_fp8_wide(tm_q, tm_w, tm_wv, tm_ok, tm_ov, a, x, sms, s));
+    }
+    if (!encode_kblocks_3d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_k_e4m3, 128, n_out,
                            kv_lora_rank / 128, static_cast<uint64_t>(kv_lora_rank), 128, 64,
                            kv_lora_rank / 128))
-        return PKM_ERR_CUDA;
+        return encode_failed();
     if (nv > 0) {
         if (!encode_kblocks_3d(&tm_wv, CU_TENSOR_MAP_DATA_TYPE_UINT8, v.w_uv, 128, nv,
                                kv_lora_rank / 128, static_cast<uint64_t>(kv_lora_rank), 128, 64,
                                kv_lora_rank / 128))
-            return PKM_ERR_CUDA;
+            return encode_failed();
     } else {
         tm_wv = tm_w;
     }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t ge = qcache != nullptr ? pkm::launch_fp8_gather_qcache(a, x, sms, s)
                                              : pkm::launch_fp8_gather_quantize(a, x, sms, s);
-    if (ge != cudaSuccess) return PKM_ERR_CUDA;
-    return pkm::launch_decompress_fp8_gemm(tm_q, tm_w, tm_wv, a, x, sms, s) == cudaSuccess
-               ? PKM_OK
-               : PKM_ERR_CUDA;
+    if (ge != cudaSuccess) return cuda_status(ge);
+    return cuda_status(pkm::launch_decompress_fp8_gemm(tm_q, tm_w, tm_wv, a, x, sms, s));
 }
 
 }  // namespace
@@ -586,10 +631,8 @@ pkm_status cache_write(const void* latent, const uint32_t* input_row_offsets, in
     a.status = dev_status;
     a.timeout_ns = wait_timeout_ns();
     int sms = 0;
-    if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
-    return pkm::launch_cache_write(a, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? PKM_OK
-               : PKM_ERR_CUDA;
+    if (const cudaError_t e = current_sm_count(&sms)) return cuda_status(e);
+    return cuda_status(pkm::launch_cache_write(a, sms, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -668,17 +711,14 @@ pkm_status kv_matmul_paged(const void* hidden_state, const uint32_t* input_row_o
     a.m_tiles = (total_rows + 255) / 256;
     a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
     int sms = 0;
-    if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
+    if (const cudaError_t e = current_sm_count(&sms)) return cuda_status(e);
     alignas(64) CUtensorMap tm_x, tm_w;
     if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, hidden_state, k_in, total_rows,
                    static_cast<uint64_t>(k_in) * 2, 64, 128) ||
         !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, weight, n_out, k_in,
                    static_cast<uint64_t>(n_out) * 2, 64, 64))
-        return PKM_ERR_CUDA;
-    return pkm::launch_kv_matmul(tm_x, tm_w, a, sms, static_cast<cudaStream_t>(stream)) ==
-                   cudaSuccess
-               ? PKM_OK
-               : PKM_ERR_CUDA;
+        return encode_failed();
+    return cuda_status(pkm::launch_kv_matmul(tm_x, tm_w, a, sms, static_cast<cudaStream_t>(stream)));
 }
 
 size_t kv_matmul_paged_fp8_workspace_size(int32_t total_rows, int32_t k_in) {
@@ -746,25 +786,20 @@ pkm_status kv_matmul_paged_fp8(const void* hidden_state, const uint32_t* input_r
         align256(static_cast<size_t>(total_rows) * static_cast<size_t>(k_in)));
     x.w_scale = w_scale;
     int sms = 0;
-    if (current_sm_count(&sms) != cudaSuccess) return PKM_ERR_CUDA;
+    if (const cudaError_t e = current_sm_count(&sms)) return cuda_status(e);
     alignas(64) CUtensorMap tm_q, tm_w;
     if (!encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.q, k_in, total_rows,
                    static_cast<uint64_t>(k_in), 128, 128) ||
         !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_e4m3, k_in, n_out,
                    static_cast<uint64_t>(k_in), 128, 128))
-        return PKM_ERR_CUDA;
-    return pkm::launch_kv_matmul_fp8(tm_q, tm_w, a, x, sms, static_cast<cudaStream_t>(stream)) ==
-                   cudaSuccess
-               ? PKM_OK
-               : PKM_ERR_CUDA;
+        return encode_failed();
+    return cuda_status(pkm::launch_kv_matmul_fp8(tm_q, tm_w, a, x, sms, static_cast<cudaStream_t>(stream)));
 }
 
 pkm_status pkm_check_wait_timeout(int32_t* dev_status, uint32_t timeout_ms, void* stream) {
     if (dev_status == nullptr || timeout_ms == 0 || timeout_ms > 5000) return PKM_ERR_INVALID_ARG;
-    return pkm::launch_wait_timeout_check(dev_status, static_cast<uint64_t>(timeout_ms) * 1000000ull,
-                                          static_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? PKM_OK
-               : PKM_ERR_CUDA;
+    return cuda_status(pkm::launch_wait_timeout_check(dev_status, static_cast<uint64_t>(timeout_ms) * 1000000ull,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

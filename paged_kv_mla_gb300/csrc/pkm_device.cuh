@@ -33,6 +33,19 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Register reallocation between warpgroups (four consecutive warps, every thread of the
+// warpgroup executes the same instruction).  The pool is what the CTA was launched with:
+// the warpgroups' new counts must add up to no more than that.
+template <int N>
+__device__ __forceinline__ void warpgroup_reg_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void warpgroup_reg_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------------------------
 // programmatic dependent launch: a prepass lets the kernel that consumes its output start
 // its prologue early; the consumer waits for the prepass's writes before reading them
@@ -98,8 +111,8 @@ struct WaitCtl {
 
 // Slow path of mbar_wait: spins until the phase completes, the abort flag rises or the wait
 // outlives timeout_ns.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
-                                                   const WaitCtl& w, bool obey_abort) {
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, const WaitCtl& w,
+                                               bool obey_abort) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -112,6 +125,12 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
             }
         }
     }
+}
+
+// The same, as a function of its own: the wait sites stay small.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                                   const WaitCtl& w, bool obey_abort) {
+    return mbar_wait_spin(bar, parity, w, obey_abort);
 }
 
 // Waits until the phase with the given parity of `bar` has completed (acquire, CTA scope).
@@ -128,6 +147,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
                                           bool obey_abort = true) {
     if (mbar_try_wait(bar, parity)) return true;
     return mbar_wait_slow(bar, parity, w, obey_abort);
+}
+
+// mbar_wait with the slow path inlined, for kernels whose warpgroups change their register
+// counts (setmaxnreg): such a region cannot call a separately compiled function.
+__device__ __forceinline__ bool mbar_wait_inl(uint64_t* bar, uint32_t parity, const WaitCtl& w,
+                                              bool obey_abort = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_spin(bar, parity, w, obey_abort);
 }
 
 // ------------------------------------------------------------------------------------
@@ -315,6 +342,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
         "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::
             "l"(reinterpret_cast<uint64_t>(map)),
         "r"(smem_u32(src)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// 3-D tiled store from this CTA's shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0,
+                                             int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::
+            "l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
 

@@ -129,6 +129,10 @@ cudaError_t launch_fp8_gather_qcache(DecompressArgs args, Fp8Extra extra, int nu
 cudaError_t launch_decompress_fp8_gemm(const CUtensorMap& tm_q, const CUtensorMap& tm_w,
                                        const CUtensorMap& tm_wv, DecompressArgs args,
                                        Fp8Extra extra, int num_sms, cudaStream_t stream);
+cudaError_t launch_decompress_fp8_wide(const CUtensorMap& tm_q, const CUtensorMap& tm_w,
+                                       const CUtensorMap& tm_wv, const CUtensorMap& tm_ok,
+                                       const CUtensorMap& tm_ov, DecompressArgs args,
+                                       Fp8Extra extra, int num_sms, cudaStream_t stream);
 cudaError_t launch_kv_matmul(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                              KvMatmulArgs args, int num_sms, cudaStream_t stream);
 cudaError_t launch_kv_matmul_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_w,

@@ -50,6 +50,8 @@ def test_status_strings(lib):
     assert lib.pkm_status_string(0) == b"PKM_OK"
     assert lib.pkm_status_string(4) == b"PKM_ERR_OUT_OF_RANGE"
     assert lib.pkm_status_string(99) == b"PKM_ERR_UNKNOWN"
+    lib.pkm_last_cuda_error.restype = ctypes.c_char_p
+    assert lib.pkm_last_cuda_error() == b"no CUDA failure recorded"
 
 
 def test_workspace_size(lib):
