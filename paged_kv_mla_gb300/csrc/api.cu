@@ -393,7 +393,7 @@ pkm_status decompress_fp8(const pkm_paged_cache* cache, uint32_t layer_idx,
     }
     a.m_tiles = (buffer_length + 255) / 256;  // CTA-pair tiles of 256 rows
     a.total_tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
-    if (wide && a.total_tiles > INT32_MAX) return PKM_ERR_UNSUPPORTED;  // 32-bit tile walk
+    if (a.total_tiles > INT32_MAX) return PKM_ERR_UNSUPPORTED;  // 32-bit tile walk
     Fp8Extra x{};
     x.q_latent = static_cast<uint8_t*>(workspace);
     x.q_scale = reinterpret_cast<float*>(

@@ -86,9 +86,6 @@ __device__ __forceinline__ bool block_tma_ok(const DecompressArgs& a, int row_bl
     return __all_sync(0xffffffffu, ok);
 }
 
-// The descriptor's start-address field counts 16-byte units: adding bytes / 16 to a
-// descriptor moves its start by that many bytes (shared addresses stay below 256 KB).
-__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decompress_fp8_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -245,9 +242,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t ad = desc_add(a_desc, static_cast<uint32_t>(kb) * kKBBytes);
+                        const uint64_t ad = desc_add_bytes(a_desc, static_cast<uint32_t>(kb) * kKBBytes);
                         const uint64_t bd =
-                            desc_add(b_desc, s * kBStageBytes + (kb - kb0) * kKBBytes);
+                            desc_add_bytes(b_desc, s * kBStageBytes + (kb - kb0) * kKBBytes);
                         const uint32_t d = tmem + acc * kBN;
 #pragma unroll
                         for (int k = 0; k < 4; ++k)

@@ -717,6 +717,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// The descriptor's start-address field counts 16-byte units: adding bytes / 16 to a
+// descriptor moves its start by that many bytes (shared addresses stay below 256 KB).
+__device__ __forceinline__ uint64_t desc_add_bytes(uint64_t d, uint32_t bytes) {
+    return d + (bytes >> 4);
+}
+
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9,
 // 10-12 = 1), A / B major-ness (bits 15 / 16: 0 = K-major, 1 = MN-major), N >> 3 at bit
 // 17, M >> 4 at bit 24.
