@@ -152,7 +152,8 @@ typedef struct {
  * r < buffer_row_offsets[0]) are left untouched.
  *
  *   cache                host struct; cache->row_elems must equal C.
- *   buffer_row_offsets   device uint32 [batch+1], non-decreasing.
+ *   buffer_row_offsets   device uint32 [batch+1], non-decreasing (not checked here;
+ *                        pkm_validate_row_offsets checks it on request).
  *   cache_offsets        device uint32 [>= batch]; entries past batch-1 are not read.
  *   buffer_length        rows of k_latent_buffer and k_buffer (>= 0; 0 launches nothing).
  *   kv_lora_rank         R: multiple of 64, 64..512.
@@ -295,7 +296,7 @@ pkm_status mla_decompress_kv_paged_fp8(const pkm_paged_cache* cache, uint32_t la
  * is written; cache_lengths are read, not updated.
  *
  *   latent          device bf16 [total_rows, R + P], row-major, 16-byte aligned.
- *   input_row_offsets  device uint32 [batch+1], non-decreasing.
+ *   input_row_offsets  device uint32 [batch+1], non-decreasing (pkm_validate_row_offsets).
  *   kv_lora_rank    R: a multiple of 8, at most 1024.
  *   rope_dim        P: a multiple of 8, at most 256.
  *   kv_norm_gamma   device fp32 [R], 16-byte aligned.
@@ -375,7 +376,12 @@ pkm_status mla_cache_write_paged_qcache(const void* latent, const uint32_t* inpu
  *     must not exceed PKM_FP8_NOALLOC_SCRATCH_BYTES (for kv_lora_rank 512: at most 31 775
  *     rows); larger calls return PKM_ERR_UNSUPPORTED and launch nothing.
  *   - Set-up: the first call on a device (with that device current) looks up the array's
- *     device address and caches it; make that first call before any stream capture.
+ *     device address and caches it; make that first call before any stream capture.  The
+ *     cached address belongs to the device's current primary context: resetting the device
+ *     (cudaDeviceReset) after the first call is not supported, since later calls would
+ *     still pass the old address.
+ *   - Status codes: the same as mla_decompress_k_paged_fp8's for the same arguments, plus
+ *     PKM_ERR_UNSUPPORTED for a call larger than the array.
  *   - Sharing: every call on a device uses the same array and leaves its contents behind.
  *     Nothing in it needs to start at zero.  Calls whose kernels overlap on the GPU (other
  *     streams, other threads) race on the array: order them on one stream or serialise them.
@@ -408,7 +414,7 @@ pkm_status mla_decompress_k_paged_fp8_noalloc(const pkm_paged_cache* cache, uint
  * with HD = cache->row_elems.  No other cache element is written.
  *
  *   hidden_state         device bf16 [total_rows, k_in], row-major, 16-byte aligned.
- *   input_row_offsets    device uint32 [batch+1], non-decreasing.
+ *   input_row_offsets    device uint32 [batch+1], non-decreasing (pkm_validate_row_offsets).
  *   total_rows           rows of hidden_state (>= 0; 0 launches nothing).
  *   k_in                 num_heads * head_size: a multiple of 64.
  *   weight               device bf16 [k_in, n_out], n_out contiguous, 16-byte aligned.
@@ -470,6 +476,28 @@ pkm_status kv_matmul_paged_fp8(const void* hidden_state, const uint32_t* input_r
  * out of range.
  */
 pkm_status pkm_check_wait_timeout(int32_t* dev_status, uint32_t timeout_ms, void* stream);
+
+/*
+ * Opt-in check of a request offset array (buffer_row_offsets, input_row_offsets).
+ * Source: generic_flare_mla_decompress_k_cache_ragged_paged -- Args buffer_row_offsets_1d,
+ * and kv_matmul_ragged_paged -- Args input_row_offsets: prefix offsets, the rows of request
+ * b being [offsets[b], offsets[b+1]).
+ *
+ * Every entry point above requires its offset array to be non-decreasing.  The kernels find
+ * a row's request by binary search, so an array that decreases somewhere yields other rows
+ * than the per-request definition; it cannot make a kernel access memory out of bounds (every
+ * lookup is range-checked), but nothing reports it.  This call launches a small kernel on
+ * `stream` that reads offsets[0 .. batch] and merges PKM_ERR_INVALID_ARG into *dev_status
+ * (device int32, required) when offsets[b] > offsets[b+1] for some b; it writes nothing else.
+ * With the environment variable PKM_DEBUG_VALIDATE=1 every entry point runs it on its own
+ * offsets (into its dev_status, when one is given) before its kernels.
+ *
+ *   offsets     device uint32 [batch + 1].
+ *   batch       >= 0 (0 launches nothing).
+ * Returns PKM_ERR_INVALID_ARG for a NULL pointer or a negative batch.
+ */
+pkm_status pkm_validate_row_offsets(const uint32_t* offsets, int32_t batch, int32_t* dev_status,
+                                    void* stream);
 
 /* Static, human-readable name of a status code. */
 const char* pkm_status_string(pkm_status status);

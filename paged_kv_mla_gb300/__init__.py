@@ -6,9 +6,20 @@ library's sm_103a kernels.  There is no CPU path: if the shared library is missi
 module refuses to import, and every call raises on a non-OK status.
 
 Entry points (same names as the C ABI in include/paged_kv_mla.h):
-  mla_decompress_k_paged       generic_flare_mla_decompress_k_cache_ragged_paged
-  mla_decompress_k_paged_fp8   the K-decompress stage of mla_prefill_decode_graph_fp8
-  kv_matmul_paged              kv_matmul_ragged_paged
+  mla_decompress_k_paged              generic_flare_mla_decompress_k_cache_ragged_paged (bf16)
+  mla_decompress_kv_paged             the same gather feeding the K and the V (w_uv) projections
+  mla_decompress_k_paged_fp8          the K-decompress stage of mla_prefill_decode_graph_fp8
+                                      (+ mla_decompress_k_paged_fp8_workspace_size)
+  mla_decompress_kv_paged_fp8         its K and V form
+  mla_decompress_k_paged_fp8_noalloc  the FP8 decompress with a fixed in-library workspace
+  mla_decompress_k_paged_fp8_qcache   the FP8 decompress reading a quantised paged cache
+  mla_cache_write_paged               RMSNorm + RoPE of new latent rows into the paged cache
+  mla_cache_write_paged_qcache        the same into a quantised paged cache
+  kv_matmul_paged                     kv_matmul_ragged_paged (bf16)
+  kv_matmul_paged_fp8                 its FP8 block-scaled form (+ kv_matmul_paged_fp8_workspace_size)
+  pkm_check_wait_timeout              the bounded-wait self-check
+  pkm_validate_row_offsets            the opt-in check that an offset array is non-decreasing
+  status_string, last_cuda_error      pkm_status_string, pkm_last_cuda_error
 """
 from __future__ import annotations
 
@@ -110,6 +121,8 @@ _lib.mla_decompress_k_paged_fp8_noalloc.restype = ctypes.c_int
 FP8_NOALLOC_SCRATCH_BYTES = 16 << 20
 _lib.pkm_check_wait_timeout.argtypes = [_vp, _u32, _vp]
 _lib.pkm_check_wait_timeout.restype = ctypes.c_int
+_lib.pkm_validate_row_offsets.argtypes = [_vp, _i32, _vp, _vp]
+_lib.pkm_validate_row_offsets.restype = ctypes.c_int
 
 
 def status_string(code: int) -> str:
@@ -400,3 +413,12 @@ __all__ = ["pkm_check_wait_timeout", "mla_decompress_k_paged_fp8_noalloc",
            "mla_decompress_k_paged_fp8_workspace_size", "fp8_workspace_views", "kv_matmul_paged",
            "status_string", "LIB_PATH", "PKM_OK", "PKM_ERR_INVALID_ARG", "PKM_ERR_UNSUPPORTED",
            "PKM_ERR_CUDA", "PKM_ERR_OUT_OF_RANGE", "PKM_ERR_TIMEOUT"]
+
+
+def pkm_validate_row_offsets(offsets: torch.Tensor, dev_status: torch.Tensor, stream=None,
+                             check: bool = True) -> int:
+    """Merges PKM_ERR_INVALID_ARG into dev_status when the offset array (batch + 1 entries)
+    decreases somewhere; writes nothing else."""
+    code = _lib.pkm_validate_row_offsets(_ptr(offsets), int(offsets.shape[0]) - 1,
+                                         _ptr(dev_status), _stream(stream))
+    return _check(code, "pkm_validate_row_offsets", check)

@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpaged_kv_mla.so")
 SOURCES = ["api.cu", "decompress_bf16.cu", "decompress_fp8.cu", "kv_matmul.cu", "selftest.cu",
            "decompress_fp8_noalloc.cu", "cache_write.cu", "kv_matmul_fp8.cu",
-           "decompress_fp8_wide.cu"]
+           "decompress_fp8_wide.cu", "validate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
@@ -33,20 +34,21 @@ uint64_t wait_timeout_ns() {
     return ns;
 }
 
-// Streaming multiprocessors of the current device (cached per device id).
+// Streaming multiprocessors of the current device, cached per device id.  Threads may race
+// to fill an entry; they all store the same value, and the atomics make that well defined.
 cudaError_t current_sm_count(int* out) {
-    static int counts[128] = {0};
+    static std::atomic<int> counts[128] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
-    if (counts[dev] == 0) {
-        int n = 0;
+    int n = counts[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        counts[dev] = n;
+        counts[dev].store(n, std::memory_order_relaxed);
     }
-    *out = counts[dev];
+    *out = n;
     return cudaSuccess;
 }
 
@@ -205,6 +207,23 @@ pkm_status encode_failed() {
     return PKM_ERR_CUDA;
 }
 
+// PKM_DEBUG_VALIDATE=1: every entry point checks its offset array on the device first
+// (pkm_validate_row_offsets into its status word, when it has one).
+bool debug_validate_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("PKM_DEBUG_VALIDATE");
+        return v != nullptr && v[0] == '1';
+    }();
+    return on;
+}
+
+cudaError_t debug_validate(const uint32_t* offsets, int32_t batch, int32_t* dev_status,
+                           void* stream) {
+    if (!debug_validate_enabled() || dev_status == nullptr || batch <= 0) return cudaSuccess;
+    return pkm::launch_validate_offsets(offsets, batch, dev_status,
+                                        static_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -303,6 +322,8 @@ pkm_status decompress_bf16(const pkm_paged_cache* cache, uint32_t layer_idx,
         !encode_cache_gather(&tm_c, a.cache_layer, cache->page_size, cache->num_pages,
                              kv_lora_rank / 64, cache->slot_stride, cache->page_stride))
         return encode_failed();
+    if (const cudaError_t e = debug_validate(buffer_row_offsets, batch, dev_status, stream))
+        return cuda_status(e);
     return cuda_status(pkm::launch_decompress_bf16(tm_w, tm_wv, tm_c, a, sms,
                                        static_cast<cudaStream_t>(stream)));
 }
@@ -430,6 +451,8 @@ pkm_status decompress_fp8(const pkm_paged_cache* cache, uint32_t layer_idx,
             tm_wv = tm_w;
             tm_ov = tm_ok;
         }
+        if (const cudaError_t e = debug_validate(buffer_row_offsets, batch, dev_status, stream))
+            return cuda_status(e);
         const cudaError_t ge = qcache != nullptr ? pkm::launch_fp8_gather_qcache(a, x, sms, s)
                                                  : pkm::launch_fp8_gather_quantize(a, x, sms, s);
         if (ge != cudaSuccess) return cuda_status(ge);
@@ -447,6 +470,8 @@ pkm_status decompress_fp8(const pkm_paged_cache* cache, uint32_t layer_idx,
     } else {
         tm_wv = tm_w;
     }
+    if (const cudaError_t e = debug_validate(buffer_row_offsets, batch, dev_status, stream))
+        return cuda_status(e);
     const cudaError_t ge = qcache != nullptr ? pkm::launch_fp8_gather_qcache(a, x, sms, s)
                                              : pkm::launch_fp8_gather_quantize(a, x, sms, s);
     if (ge != cudaSuccess) return cuda_status(ge);
@@ -632,6 +657,8 @@ pkm_status cache_write(const void* latent, const uint32_t* input_row_offsets, in
     a.timeout_ns = wait_timeout_ns();
     int sms = 0;
     if (const cudaError_t e = current_sm_count(&sms)) return cuda_status(e);
+    if (const cudaError_t e = debug_validate(a.row_offsets, batch, dev_status, stream))
+        return cuda_status(e);
     return cuda_status(pkm::launch_cache_write(a, sms, static_cast<cudaStream_t>(stream)));
 }
 
@@ -718,6 +745,8 @@ pkm_status kv_matmul_paged(const void* hidden_state, const uint32_t* input_row_o
         !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, weight, n_out, k_in,
                    static_cast<uint64_t>(n_out) * 2, 64, 64))
         return encode_failed();
+    if (const cudaError_t e = debug_validate(a.row_offsets, a.batch, a.status, stream))
+        return cuda_status(e);
     return cuda_status(pkm::launch_kv_matmul(tm_x, tm_w, a, sms, static_cast<cudaStream_t>(stream)));
 }
 
@@ -793,7 +822,17 @@ pkm_status kv_matmul_paged_fp8(const void* hidden_state, const uint32_t* input_r
         !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_e4m3, k_in, n_out,
                    static_cast<uint64_t>(k_in), 128, 128))
         return encode_failed();
+    if (const cudaError_t e = debug_validate(a.row_offsets, a.batch, a.status, stream))
+        return cuda_status(e);
     return cuda_status(pkm::launch_kv_matmul_fp8(tm_q, tm_w, a, x, sms, static_cast<cudaStream_t>(stream)));
+}
+
+pkm_status pkm_validate_row_offsets(const uint32_t* offsets, int32_t batch, int32_t* dev_status,
+                                    void* stream) {
+    if (offsets == nullptr || dev_status == nullptr || batch < 0) return PKM_ERR_INVALID_ARG;
+    if (batch == 0) return PKM_OK;
+    return cuda_status(pkm::launch_validate_offsets(offsets, batch, dev_status,
+                                                    static_cast<cudaStream_t>(stream)));
 }
 
 pkm_status pkm_check_wait_timeout(int32_t* dev_status, uint32_t timeout_ms, void* stream) {

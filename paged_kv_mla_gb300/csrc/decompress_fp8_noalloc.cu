@@ -12,7 +12,9 @@
 //
 // Host code cannot use the array's name as a device pointer (on the host it names a
 // stand-in object).  The device address is looked up with cudaGetSymbolAddress once per
-// device, on the first call made while that device is current, and cached.
+// device, on the first call made while that device is current, and cached; it is not
+// looked up again, so the device's context must outlive the calls (no cudaDeviceReset
+// after the first one).
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -61,10 +63,27 @@ pkm_status mla_decompress_k_paged_fp8_noalloc(const pkm_paged_cache* cache, uint
                                               const float* w_k_scale, int32_t n_out,
                                               void* k_latent_buffer, void* k_buffer,
                                               int32_t* dev_status, void* stream) {
-    if (buffer_length < 0 || batch < 0) return PKM_ERR_INVALID_ARG;
-    if (buffer_length == 0 || batch == 0) return PKM_OK;
+    // The status codes follow mla_decompress_k_paged_fp8's order of checks: invalid sizes,
+    // then calls with nothing to do, then everything else.  Those first two never touch
+    // the workspace, so they go to that entry point without one.
+    const bool bad_sizes = batch < 0 || buffer_length < 0 || rope_dim < 0 || n_out <= 0 ||
+                           kv_lora_rank <= 0;
+    if (bad_sizes || batch == 0 || buffer_length == 0)
+        return mla_decompress_k_paged_fp8(cache, layer_idx, buffer_row_offsets, cache_offsets,
+                                          batch, buffer_length, kv_lora_rank, rope_dim, w_k_e4m3,
+                                          w_k_scale, n_out, k_latent_buffer, k_buffer, nullptr, 0,
+                                          dev_status, stream);
     const size_t need = mla_decompress_k_paged_fp8_workspace_size(buffer_length, kv_lora_rank);
-    if (need == 0) return PKM_ERR_UNSUPPORTED;            // kv_lora_rank not a multiple of 128
+    if (need == 0) {
+        // kv_lora_rank is not a multiple of 128: the regular entry point rejects the call
+        // (pointer checks first, then the unsupported rank) before it would touch a
+        // workspace, so a stand-in that is never dereferenced takes the workspace's place
+        alignas(256) static unsigned char stand_in[256];
+        return mla_decompress_k_paged_fp8(cache, layer_idx, buffer_row_offsets, cache_offsets,
+                                          batch, buffer_length, kv_lora_rank, rope_dim, w_k_e4m3,
+                                          w_k_scale, n_out, k_latent_buffer, k_buffer, stand_in,
+                                          sizeof(stand_in), dev_status, stream);
+    }
     if (need > kScratchBytes) return PKM_ERR_UNSUPPORTED;  // more rows than the fixed scratch holds
     void* scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess) return PKM_ERR_CUDA;

@@ -140,6 +140,8 @@ cudaError_t launch_kv_matmul_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_
                                  cudaStream_t stream);
 cudaError_t launch_cache_write(CacheWriteArgs args, int num_sms, cudaStream_t stream);
 cudaError_t launch_wait_timeout_check(int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+cudaError_t launch_validate_offsets(const uint32_t* offsets, int32_t batch, int32_t* status,
+                                    cudaStream_t stream);
 
 // Row bookkeeping shared by the decompress kernels: element offset (inside the layer) of
 // the cache slot that feeds output row r, -1 when no request covers r (or r >= row_end),

@@ -182,3 +182,55 @@ def test_oracle_and_product_share_no_code():
             assert "oracle" not in open(f).read().lower(), f
     src = open(os.path.join(ROOT, "oracle", "pkm_oracle.c")).read()
     assert "#include \"" not in src and "paged_kv_mla" not in src
+
+
+def test_noalloc_status_codes_match_the_workspace_entry_point_without_a_gpu(lib):
+    """Argument errors of the allocation-free FP8 call return what mla_decompress_k_paged_fp8
+    returns for the same arguments (it checks sizes first, then does nothing for an empty
+    call, then checks pointers and the rank); none of these calls touches the GPU."""
+    import torch
+    import paged_kv_mla_gb300 as pkm
+    t16 = torch.zeros(1024, dtype=torch.int16)
+    raw = torch.zeros(1 << 16, dtype=torch.uint8)
+    off = (-raw.data_ptr()) % 256
+    ws = raw[off:off + (1 << 15)]                  # a 256-byte-aligned host stand-in
+    ws_scale = torch.ones(4, dtype=torch.float32)
+    co = torch.zeros(2, dtype=torch.int32)
+
+    def both(cache, bro, L, R, P, n_out, lat=t16, kb=t16):
+        w = torch.zeros(max(n_out, 0) * max(R, 1), dtype=torch.uint8).view(max(n_out, 0), max(R, 1))
+        a = pkm.mla_decompress_k_paged_fp8(cache, 0, bro, co, L, R, P, w, ws_scale, lat, kb, ws,
+                                           stream=0, check=False)
+        b = pkm.mla_decompress_k_paged_fp8_noalloc(cache, 0, bro, co, L, R, P, w, ws_scale, lat,
+                                                   kb, stream=0, check=False)
+        return a, b
+
+    one = torch.tensor([0, 4], dtype=torch.int32)
+    none = torch.tensor([0], dtype=torch.int32)     # batch 0
+    good = _cache(pkm)                             # row_elems 80 = 64 + 16
+    cases = [
+        (good, none, 4, 64, 16, 0, pkm.PKM_ERR_INVALID_ARG),    # n_out 0, nothing to do
+        (good, one, 0, 0, 16, 128, pkm.PKM_ERR_INVALID_ARG),    # rank 0, no rows
+        (good, one, 0, 64, -1, 128, pkm.PKM_ERR_INVALID_ARG),   # negative rope_dim
+        (good, one, -1, 64, 16, 128, pkm.PKM_ERR_INVALID_ARG),  # negative length
+        (good, none, 4, 64, 16, 128, pkm.PKM_OK),               # no requests
+        (good, one, 0, 64, 16, 128, pkm.PKM_OK),                # no rows
+        (good, one, 4, 64, 16, 128, pkm.PKM_ERR_UNSUPPORTED),   # rank not a multiple of 128
+        (_cache(pkm, num_pages=0), one, 4, 64, 16, 128, pkm.PKM_ERR_INVALID_ARG),
+    ]
+    for cache, bro, L, R, P, n_out, want in cases:
+        assert both(cache, bro, L, R, P, n_out) == (want, want), (L, R, P, n_out)
+    a, b = both(good, one, 4, 64, 16, 128, kb=t16[1:])     # misaligned output
+    assert a == b == pkm.PKM_ERR_INVALID_ARG
+
+
+def test_offset_check_arguments_without_a_gpu(lib):
+    import torch
+    import paged_kv_mla_gb300 as pkm
+    st = torch.zeros(1, dtype=torch.int32)
+    assert pkm.pkm_validate_row_offsets(torch.zeros(1, dtype=torch.int32), st, stream=0,
+                                        check=False) == pkm.PKM_OK        # batch 0
+    assert lib.pkm_validate_row_offsets(None, 3, st.data_ptr(), None) == pkm.PKM_ERR_INVALID_ARG
+    assert lib.pkm_validate_row_offsets(st.data_ptr(), 3, None, None) == pkm.PKM_ERR_INVALID_ARG
+    assert lib.pkm_validate_row_offsets(st.data_ptr(), -1, st.data_ptr(), None) == pkm.PKM_ERR_INVALID_ARG
+

@@ -295,17 +295,37 @@ def test_kv_matmul_write_path_full_size():
     expect[dest // E] = True
     changed = (out[0] != k.cache[0]).any(axis=-1).reshape(2, P * S)
     assert np.array_equal(changed[0], expect) and np.array_equal(changed[1], expect)
-    # values of three whole requests against the oracle on that sub-batch
-    pick = [0, 13, 31]
+    # values of sampled rows of EVERY request against the oracle: each request's first and
+    # last new row, the rows on both sides of every page boundary its new tokens cross, and
+    # four seeded random rows.  Each sampled row becomes a one-row request of its own with
+    # the same page table row and cache position, so the oracle writes the same slot.
+    rng = np.random.default_rng(29)
     iro = k.input_row_offsets.astype(np.int64)
-    rows = np.concatenate([np.arange(iro[b], iro[b + 1]) for b in pick])
+    ps = k.page_size
+    sel = []
+    for b in range(k.batch):
+        n = int(iro[b + 1] - iro[b])
+        if n == 0:
+            continue
+        cl = int(k.cache_lengths[b])
+        picks = {0, n - 1}
+        for i in range(1, n):
+            if (cl + i) % ps == 0:
+                picks.update({i - 1, i})
+        picks.update(int(v) for v in rng.integers(0, n, 4))
+        sel.extend((b, i) for i in sorted(picks))
+    assert len({b for b, _ in sel}) == int((iro[1:] > iro[:-1]).sum())
+    rows = np.array([iro[b] + i for b, i in sel])
     sub = workloads.KvMatmulInputs(
         name="sub", hidden_state=k.hidden_state[rows],
-        input_row_offsets=np.concatenate([[0], np.cumsum([iro[b + 1] - iro[b] for b in pick])]).astype(np.uint32),
-        weight=k.weight, cache=k.cache, page_table=k.page_table[pick],
-        cache_lengths=k.cache_lengths[pick], head_elems=k.head_elems, layer_idx=k.layer_idx)
+        input_row_offsets=np.arange(len(sel) + 1, dtype=np.uint32),
+        weight=k.weight, cache=k.cache, page_table=k.page_table[[b for b, _ in sel]],
+        cache_lengths=np.array([int(k.cache_lengths[b]) + i for b, i in sel], np.uint32),
+        head_elems=k.head_elems, layer_idx=k.layer_idx)
     st, ref = oracle_kv_matmul(sub)
+    assert st == 0
     changed_ref = ref != k.cache
+    assert changed_ref.sum() == len(sel) * 2 * k.head_elems  # K and V slot of each row
     assert_close_bf16(out[changed_ref], ref[changed_ref], BF16_TOL, "kv cache values")
 
 

@@ -3,10 +3,12 @@ regular FP8 entry point.
 
 The no-alloc call is for callers that cannot allocate device memory (an engine plug-in that
 only receives pre-planned buffers, a serving loop that must not call cudaMalloc); it keeps
-its quantised latent in a fixed device array inside the library.  Its results must match
-mla_decompress_k_paged_fp8 with a caller workspace, on two calls in a row (the second call
-reuses the array the first one left behind).  This file is collected last so a stop-at-first-
-failure run has already run every other test; it also passes alone in a fresh process."""
+its quantised latent in a fixed device array inside the library.  Both calls run the same
+deterministic kernels on the same inputs, so its outputs must equal those of
+mla_decompress_k_paged_fp8 with a caller workspace bit for bit, on two calls in a row (the
+second call reuses the array the first one left behind); once, they are also checked against
+the CPU oracle.  This file is collected last so a stop-at-first-failure run has already run
+every other test; it also passes alone in a fresh process."""
 from __future__ import annotations
 
 import numpy as np
@@ -15,6 +17,7 @@ import torch
 
 import workloads
 from gpu_util import FP8_TOL, DeviceDecompress, _i16, assert_close_bf16, host_u16
+from util import oracle_decompress_fp8
 
 pytestmark = pytest.mark.gpu
 
@@ -56,8 +59,13 @@ def test_noalloc_matches_the_workspace_entry_point_twice(seed, lengths, offsets,
         code, lat, kb, st = _noalloc_run(g)
         assert code == pkm.PKM_OK and st == 0
         assert np.array_equal(lat, ref_lat)
-        assert (kb == workloads.SENTINEL_OUT).sum() == (ref_kb == workloads.SENTINEL_OUT).sum()
-        assert_close_bf16(kb, ref_kb, FP8_TOL, "no-alloc k_buffer")
+        assert np.array_equal(kb, ref_kb), "no-alloc k_buffer differs from the workspace call"
+    if seed == 701:  # and once against the oracle (dequantised-value fp64 product)
+        ost, olat, ok, oq, os_, written = oracle_decompress_fp8(d)
+        assert ost == 0
+        assert np.array_equal(lat[written], olat[written])
+        assert_close_bf16(kb[written], ok[written], FP8_TOL, "no-alloc k_buffer vs oracle")
+        assert (kb[~written] == workloads.SENTINEL_OUT).all()
 
 
 def test_noalloc_rejects_more_rows_than_its_scratch_holds():
