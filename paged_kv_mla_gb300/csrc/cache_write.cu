@@ -278,14 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int sh = 8; sh >= 1; sh >>= 1)
                             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
-                        const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+                        const E4m3Block qb(amax);
+                        const float s = qb.s;
                         if (c < nope_chunks) {
-                            const uint32_t lo =
-                                e4m3x2(__fdiv_rn(y[0], s), __fdiv_rn(y[1], s)) |
-                                (e4m3x2(__fdiv_rn(y[2], s), __fdiv_rn(y[3], s)) << 16);
-                            const uint32_t hi =
-                                e4m3x2(__fdiv_rn(y[4], s), __fdiv_rn(y[5], s)) |
-                                (e4m3x2(__fdiv_rn(y[6], s), __fdiv_rn(y[7], s)) << 16);
+                            const uint32_t lo = qb.codes4(y[0], y[1], y[2], y[3]);
+                            const uint32_t hi = qb.codes4(y[4], y[5], y[6], y[7]);
                             *reinterpret_cast<uint2*>(dstq + c * 8) = make_uint2(lo, hi);
                             if ((lane & 15) == 0)
                                 *reinterpret_cast<float*>(dstq + R + 2 * P + 4 * (c / 16)) = s;

@@ -94,13 +94,13 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
             for (int sh = 4; sh >= 1; sh >>= 1)  // the eight lanes of one block
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
-            const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+            const E4m3Block qb(amax);
+            const float s = qb.s;
             if (!nope) continue;
             uint32_t o[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                o[i] = e4m3x2(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s)) |
-                       (e4m3x2(__fdiv_rn(f[4 * i + 2], s), __fdiv_rn(f[4 * i + 3], s)) << 16);
+                o[i] = qb.codes4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
             st_v4(x.q_latent + r * R + lane * 16, make_uint4(o[0], o[1], o[2], o[3]));
             if ((lane & 7) == 0) x.q_scale[r * kblocks + lane / 8] = s;
         }
