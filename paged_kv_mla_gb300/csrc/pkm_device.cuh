@@ -524,11 +524,11 @@ __device__ __forceinline__ void warp_store_rows_32x64(uint32_t stage, const uint
     __syncwarp();  // the box may be overwritten once every lane has read its part
 }
 
-// x / s for a block scale s > 0 whose correctly rounded reciprocal y = RN(1 / s) the
-// caller computes once per block: the remainder correction of Markstein (IBM J. Res.
-// Develop. 34(1), 1990).  q0 = RN(x * y) is within an ulp of x / s, so the remainder
-// r = x - q0 * s is exact in one FMA, and RN(q0 + r * y) is RN(x / s) or its neighbour.
-// The sign of a zero quotient is the sign of x.
+// x / s for a block scale s > 0 with an approximate reciprocal y ~ 1 / s (within an ulp or
+// so) that the caller computes once per block: the remainder correction of Markstein (IBM
+// J. Res. Develop. 34(1), 1990).  q0 = RN(x * y) is within a few ulps of x / s, the
+// remainder r = x - q0 * s is exact in one FMA, and RN(q0 + r * y) is RN(x / s) or its
+// neighbour.  The sign of a zero quotient is the sign of x.
 __device__ __forceinline__ float div_by_scale(float x, float s, float y) {
     const float q0 = __fmul_rn(x, y);
     const float r = __fmaf_rn(-q0, s, x);
@@ -545,15 +545,24 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 
 // One 128-value block quantised to e4m3: s = RN(amax / 448) (1 for an all-zero block) and
 // codes e4m3_rne_satfinite(RN(x / s)) for |x| <= amax, x and amax bf16 values.  For
-// amax >= 2^-100 the quotient comes from div_by_scale: it can miss RN(x / s) by one ulp, but
-// never where that changes the e4m3 code (checked exhaustively over every bf16 x and amax;
-// code differences appear only for amax < 2^-104).  Smaller blocks divide correctly rounded.
+// amax >= 2^-100 the quotient comes from div_by_scale with the hardware's approximate
+// reciprocal: it can miss RN(x / s) by an ulp, but never where that changes the e4m3 code
+// (checked exhaustively over every bf16 x and amax; code differences appear only for
+// amax < 2^-104).  Smaller blocks divide correctly rounded.  The scale itself is always the
+// correctly rounded quotient: amax * RN(1 / 448) differs from it for about half the bf16
+// values of amax.
+__device__ __forceinline__ float rcp_approx(float s) {
+    float y;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(s));
+    return y;
+}
+
 struct E4m3Block {
     float s, y;
     bool fast;
     __device__ __forceinline__ explicit E4m3Block(float amax) {
         s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-        y = __frcp_rn(s);
+        y = rcp_approx(s);
         fast = amax >= 0x1p-100f;
     }
     // codes of four values, the first in the low byte
