@@ -26,8 +26,8 @@
 // Into a quantised cache (PagedKVCacheCollection's scale_dtype_ / quantization_granularity_)
 // the rounded bf16 values of each 128-column block are quantised on the spot, the block
 // being the 16 chunks of one half-warp: s = amax / 448 (fp32), codes e4m3_rne_satfinite(y / s)
-// with the division in fp32, correctly rounded; the slot gets the codes, the bf16 rope
-// columns and the scales.
+// with the codes of the correctly rounded fp32 quotient; the slot gets the codes, the bf16
+// rope columns and the scales.
 #include "pkm_device.cuh"
 #include "pkm_internal.h"
 
@@ -231,17 +231,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.empty[p.stage]);
             p.next(stages);
+            bool ok[U];
+            int64_t doff[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                if (slot[u] < 0 || page[u] >= static_cast<uint32_t>(a.num_pages)) {
-                    if ((slot[u] == kSlotOutOfRange || slot[u] >= 0) && lane == 0)
-                        report(a.status, PKM_ERR_OUT_OF_RANGE);
-                    continue;
-                }
-                const int64_t doff = static_cast<int64_t>(page[u]) * a.page_stride +
-                                     static_cast<int64_t>(slot[u]) * a.slot_stride;
-                uint16_t* dst = QUANT ? nullptr : a.cache_layer + doff;
-                uint8_t* dstq = QUANT ? a.qcache_layer + doff : nullptr;
+                ok[u] = slot[u] >= 0 && page[u] < static_cast<uint32_t>(a.num_pages);
+                if (!ok[u] && (slot[u] == kSlotOutOfRange || slot[u] >= 0) && lane == 0)
+                    report(a.status, PKM_ERR_OUT_OF_RANGE);
+                doff[u] = static_cast<int64_t>(page[u]) * a.page_stride +
+                          static_cast<int64_t>(max(slot[u], 0)) * a.slot_stride;
+            }
+            // RMSNorm factor of each row (rows that are not stored compute on zeros); the
+            // rows go through every step side by side, so that their latencies overlap
+            float inv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
                 float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
                 for (int j = 0; j < NC; ++j) {
@@ -251,79 +255,104 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 4; ++i)
                         fma2v(s0, s1, f[2 * i], f[2 * i + 1], f[2 * i], f[2 * i + 1]);
                 }
-                float ss = s0 + s1;
+                inv[u] = s0 + s1;
+            }
 #pragma unroll
-                for (int sh = 16; sh >= 1; sh >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, sh);
-                const float inv = rsqrtf(fmaf(ss, inv_r, a.epsilon));
-                if constexpr (QUANT) {
-                    // round to bf16 as the bf16 cache would, then quantise each 128-column
-                    // block (16 chunks = one half-warp): s = amax / 448, q = e4m3(y / s)
+            for (int sh = 16; sh >= 1; sh >>= 1)
 #pragma unroll
-                    for (int j = 0; j < NC; ++j) {
-                        const int c = lane + 32 * j;
-                        float f[8], y[8];
+                for (int u = 0; u < U; ++u) inv[u] += __shfl_xor_sync(0xffffffffu, inv[u], sh);
+#pragma unroll
+            for (int u = 0; u < U; ++u) inv[u] = rsqrtf(fmaf(inv[u], inv_r, a.epsilon));
+            if constexpr (QUANT) {
+                // round to bf16 as the bf16 cache would, then quantise each 128-column block
+                // (16 chunks = one half-warp): s = amax / 448, q = e4m3(y / s).  The two
+                // half-warps' block maxima come from two whole-warp reductions in which the
+                // other half contributes zero.
+#pragma unroll
+                for (int j = 0; j < NC; ++j) {
+                    const int c = lane + 32 * j;
+                    float y[U][8];
+                    uint32_t mlo[U], mhi[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        float f[8];
                         unpack8(nv[u][j], f);
+                        float m = 0.0f;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             float g0, g1, y0, y1;
-                            mul2(g0, g1, gr[j][2 * i], gr[j][2 * i + 1], inv, inv);
+                            mul2(g0, g1, gr[j][2 * i], gr[j][2 * i + 1], inv[u], inv[u]);
                             mul2(y0, y1, f[2 * i], f[2 * i + 1], g0, g1);
                             const uint32_t pk = pack_bf16x2(y0, y1);
-                            y[2 * i] = __uint_as_float(pk << 16);
-                            y[2 * i + 1] = __uint_as_float(pk & 0xFFFF0000u);
+                            y[u][2 * i] = __uint_as_float(pk << 16);
+                            y[u][2 * i + 1] = __uint_as_float(pk & 0xFFFF0000u);
+                            m = fmaxf(m, fmaxf(fabsf(y[u][2 * i]), fabsf(y[u][2 * i + 1])));
                         }
-                        float amax = 0.0f;
+                        const uint32_t mb = __float_as_uint(m);
+                        mlo[u] = lane < 16 ? mb : 0u;
+                        mhi[u] = lane < 16 ? 0u : mb;
+                    }
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(y[i]));
+                    for (int u = 0; u < U; ++u) {
+                        mlo[u] = warp_max_u32(mlo[u]);
+                        mhi[u] = warp_max_u32(mhi[u]);
+                    }
 #pragma unroll
-                        for (int sh = 8; sh >= 1; sh >>= 1)
-                            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
-                        const E4m3Block qb(amax);
-                        const float s = qb.s;
-                        if (c < nope_chunks) {
-                            const uint32_t lo = qb.codes4(y[0], y[1], y[2], y[3]);
-                            const uint32_t hi = qb.codes4(y[4], y[5], y[6], y[7]);
+                    for (int u = 0; u < U; ++u) {
+                        const E4m3Block qb(__uint_as_float(lane < 16 ? mlo[u] : mhi[u]));
+                        const uint32_t lo = qb.codes4(y[u][0], y[u][1], y[u][2], y[u][3]);
+                        const uint32_t hi = qb.codes4(y[u][4], y[u][5], y[u][6], y[u][7]);
+                        if (ok[u] && c < nope_chunks) {
+                            uint8_t* dstq = a.qcache_layer + doff[u];
                             *reinterpret_cast<uint2*>(dstq + c * 8) = make_uint2(lo, hi);
                             if ((lane & 15) == 0)
-                                *reinterpret_cast<float*>(dstq + R + 2 * P + 4 * (c / 16)) = s;
+                                *reinterpret_cast<float*>(dstq + R + 2 * P + 4 * (c / 16)) = qb.s;
                         }
                     }
                 }
+            } else {
 #pragma unroll
-                for (int j = 0; j < NC && !QUANT; ++j) {
-                    const int c = lane + 32 * j;
-                    if (c >= nope_chunks) break;
-                    float f[8];
-                    unpack8(nv[u][j], f);
-                    uint32_t o[4];
+                for (int u = 0; u < U; ++u) {
+                    if (!ok[u]) continue;
+                    uint16_t* dst = a.cache_layer + doff[u];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float g0, g1, y0, y1;
-                        mul2(g0, g1, gr[j][2 * i], gr[j][2 * i + 1], inv, inv);
-                        mul2(y0, y1, f[2 * i], f[2 * i + 1], g0, g1);
-                        o[i] = pack_bf16x2(y0, y1);
+                    for (int j = 0; j < NC; ++j) {
+                        const int c = lane + 32 * j;
+                        if (c >= nope_chunks) break;
+                        float f[8];
+                        unpack8(nv[u][j], f);
+                        uint32_t o[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float g0, g1, y0, y1;
+                            mul2(g0, g1, gr[j][2 * i], gr[j][2 * i + 1], inv[u], inv[u]);
+                            mul2(y0, y1, f[2 * i], f[2 * i + 1], g0, g1);
+                            o[i] = pack_bf16x2(y0, y1);
+                        }
+                        st_v4(dst + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
                     }
-                    st_v4(dst + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
                 }
-                if (has_rope) {
-                    float f[8];
-                    unpack8(rv[u], f);
-                    const float cs[8] = {__uint_as_float(fq[u][0].x), __uint_as_float(fq[u][0].y),
-                                         __uint_as_float(fq[u][0].z), __uint_as_float(fq[u][0].w),
-                                         __uint_as_float(fq[u][1].x), __uint_as_float(fq[u][1].y),
-                                         __uint_as_float(fq[u][1].z), __uint_as_float(fq[u][1].w)};
-                    uint32_t o[4];
+            }
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {  // pair i: (x0, x1) by (cos, sin)
-                        const float x0 = f[2 * i], x1 = f[2 * i + 1];
-                        const float c = cs[2 * i], s = cs[2 * i + 1];
-                        o[i] = pack_bf16x2(fmaf(x0, c, -x1 * s), fmaf(x0, s, x1 * c));
-                    }
-                    if constexpr (QUANT)
-                        st_v4(dstq + R + lane * 16, make_uint4(o[0], o[1], o[2], o[3]));
-                    else
-                        st_v4(dst + R + lane * 8, make_uint4(o[0], o[1], o[2], o[3]));
+            for (int u = 0; u < U; ++u) {
+                if (!ok[u] || !has_rope) continue;
+                float f[8];
+                unpack8(rv[u], f);
+                const float cs[8] = {__uint_as_float(fq[u][0].x), __uint_as_float(fq[u][0].y),
+                                     __uint_as_float(fq[u][0].z), __uint_as_float(fq[u][0].w),
+                                     __uint_as_float(fq[u][1].x), __uint_as_float(fq[u][1].y),
+                                     __uint_as_float(fq[u][1].z), __uint_as_float(fq[u][1].w)};
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {  // pair i: (x0, x1) by (cos, sin)
+                    const float x0 = f[2 * i], x1 = f[2 * i + 1];
+                    const float c = cs[2 * i], s = cs[2 * i + 1];
+                    o[i] = pack_bf16x2(fmaf(x0, c, -x1 * s), fmaf(x0, s, x1 * c));
                 }
+                if constexpr (QUANT)
+                    st_v4(a.qcache_layer + doff[u] + R + lane * 16, make_uint4(o[0], o[1], o[2], o[3]));
+                else
+                    st_v4(a.cache_layer + doff[u] + R + lane * 8, make_uint4(o[0], o[1], o[2], o[3]));
             }
         }
     }

@@ -9,8 +9,9 @@
 // (fp8_gather_quantize_kernel or fp8_gather_qcache_kernel); this kernel is launched as its
 // programmatic dependent.  With w_uv the V tiles follow the K tiles of each row block.
 //
-// Clusters of two CTAs (a CTA pair) walk 256 x 256 output tiles: a pair MMA with N = 256
-// keeps the e4m3 tensor pipe at its full rate (N = 128 pair MMAs run at about half of it).
+// Clusters of two CTAs (a CTA pair) walk 256 x 256 output tiles: every k-block's
+// accumulator has to leave TMEM before its slot is reused, and with N = 256 one such
+// hand-off covers twice the output columns it covers with N = 128.
 // Each CTA keeps its 128 quantised rows resident (one 16 KB TMA box per 128-wide k-block,
 // refilled k-block by k-block when the pair moves to its next row block) and streams its
 // 128-row half of each tile's weight slice k-block by k-block through a TMA ring.  Every
@@ -19,9 +20,10 @@
 // (two of 256 columns), and 16 epilogue warps per CTA (32 rows x 64 columns each) fold it
 // into fp32 running sums, s_a * s_w * partial, handing the accumulator back as soon as it
 // is read, so the MMAs of the next k-block run meanwhile.  After a tile's last k-block each
-// warp rounds its sums to bf16 into a 128-byte-swizzled 4 KB shared box and one lane
-// stores the box with an asynchronous TMA store (rows past buffer_length are clipped by
-// the tensor map); a box holding a row that must stay untouched is stored row by row.
+// warp rounds its sums to bf16 into its 128-byte-swizzled 32 x 64 part of a 64 KB shared
+// box, and a store thread writes the CTA's whole 128 x 256 tile with one 3-D TMA store
+// (rows past buffer_length are clipped by the tensor map); a row block with rows that must
+// stay untouched is stored row by row by the epilogue warps instead.
 #include "pkm_device.cuh"
 #include "pkm_internal.h"
 

@@ -14,8 +14,9 @@
 //      workspace (codes [M, k_in]; scales k-block-major, [k_in / 128, M], so that the
 //      epilogue's per-k-block scale loads of 32 consecutive rows are one 128-byte line).
 //   2. kv_matmul_fp8_kernel: clusters of two CTAs over 256 x 256 output tiles (two
-//      weight-scale blocks; N = 256 keeps the e4m3 MMAs at full rate, where N = 128 ran at
-//      about half).  Each CTA streams, per 128-wide k-block, its 128 rows of quantised A and
+//      weight-scale blocks; one accumulator hand-off per k-block then covers 256 output
+//      columns, twice as many as with N = 128, and the hand-off, not the MMA rate, bounds
+//      this GEMM).  Each CTA streams, per 128-wide k-block, its 128 rows of quantised A and
 //      its 128-row half of the weight through a 5-stage TMA ring; the even CTA issues
 //      tcgen05.mma.cta_group::2 kind::f8f6f4 (M = 256) into one of two 256-column TMEM
 //      accumulators.  Because every k-block carries its own scales, 16 epilogue warps per

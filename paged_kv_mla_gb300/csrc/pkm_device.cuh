@@ -524,17 +524,14 @@ __device__ __forceinline__ void warp_store_rows_32x64(uint32_t stage, const uint
     __syncwarp();  // the box may be overwritten once every lane has read its part
 }
 
-// x / s for a block scale s > 0 with an approximate reciprocal y ~ 1 / s (within an ulp or
-// so) that the caller computes once per block: the remainder correction of Markstein (IBM
-// J. Res. Develop. 34(1), 1990).  q0 = RN(x * y) is within a few ulps of x / s, the
-// remainder r = x - q0 * s is exact in one FMA, and RN(q0 + r * y) is RN(x / s) or its
-// neighbour.  The sign of a zero quotient is the sign of x.
-__device__ __forceinline__ float div_by_scale(float x, float s, float y) {
-    const float q0 = __fmul_rn(x, y);
-    const float r = __fmaf_rn(-q0, s, x);
-    return copysignf(__fmaf_rn(r, y, q0), x);
+// Maximum of v over the 32 lanes of a warp, in one instruction (every lane must execute it).
+// For non-negative floats the bit patterns order like the values, so this also takes the
+// maximum of magnitudes.
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+    uint32_t r;
+    asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
 }
-
 
 // Two fp32 values to e4m3 (round to nearest even, saturating to +-448); lo in the low byte.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
@@ -542,38 +539,6 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     return r;
 }
-
-// One 128-value block quantised to e4m3: s = RN(amax / 448) (1 for an all-zero block) and
-// codes e4m3_rne_satfinite(RN(x / s)) for |x| <= amax, x and amax bf16 values.  For
-// amax >= 2^-100 the quotient comes from div_by_scale with the hardware's approximate
-// reciprocal: it can miss RN(x / s) by an ulp, but never where that changes the e4m3 code
-// (checked exhaustively over every bf16 x and amax; code differences appear only for
-// amax < 2^-104).  Smaller blocks divide correctly rounded.  The scale itself is always the
-// correctly rounded quotient: amax * RN(1 / 448) differs from it for about half the bf16
-// values of amax.
-__device__ __forceinline__ float rcp_approx(float s) {
-    float y;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(s));
-    return y;
-}
-
-struct E4m3Block {
-    float s, y;
-    bool fast;
-    __device__ __forceinline__ explicit E4m3Block(float amax) {
-        s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-        y = rcp_approx(s);
-        fast = amax >= 0x1p-100f;
-    }
-    // codes of four values, the first in the low byte
-    __device__ __forceinline__ uint32_t codes4(float a, float b, float c, float d) const {
-        if (fast)
-            return e4m3x2(div_by_scale(a, s, y), div_by_scale(b, s, y)) |
-                   (e4m3x2(div_by_scale(c, s, y), div_by_scale(d, s, y)) << 16);
-        return e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s)) |
-               (e4m3x2(__fdiv_rn(c, s), __fdiv_rn(d, s)) << 16);
-    }
-};
 
 // (d0, d1) += (a0, a1) * (b0, b1), one packed fp32x2 FMA (each lane rounded as fmaf).
 __device__ __forceinline__ void fma2v(float& d0, float& d1, float a0, float a1, float b0,
@@ -604,6 +569,85 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
     return *reinterpret_cast<uint32_t*>(&h);
 }
+
+// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1), one packed fp32x2 FMA (each lane as fmaf).
+__device__ __forceinline__ void fma2x(float& d0, float& d1, float a0, float a1, float b0,
+                                      float b1, float c0, float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rc;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+__device__ __forceinline__ float rcp_approx(float s) {
+    float y;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(s));
+    return y;
+}
+
+// x / s for a block scale s > 0 with an approximate reciprocal y ~ 1 / s (within an ulp or
+// so) that the caller computes once per block: the remainder correction of Markstein (IBM
+// J. Res. Develop. 34(1), 1990).  q0 = RN(x * y) is within a few ulps of x / s, the
+// remainder r = x - q0 * s is exact in one FMA, and RN(q0 + r * y) is RN(x / s) or its
+// neighbour.  The sign of a zero quotient is the sign of x.
+__device__ __forceinline__ float div_by_scale(float x, float s, float y) {
+    const float q0 = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q0, s, x);
+    return copysignf(__fmaf_rn(r, y, q0), x);
+}
+
+// RN(amax / 448) for amax >= 2^-100 (a normal quotient): the same correction with the
+// correctly rounded constant c = RN(1 / 448), q0 = RN(amax * c), r = amax - 448 * q0
+// (exact), RN(q0 + r * c).  Checked equal to the correctly rounded quotient for every
+// bf16 amax in that range.
+__device__ __forceinline__ float scale_of_amax(float amax) {
+    const float c = 0x1.24924ap-9f;  // RN(1 / 448)
+    const float q0 = __fmul_rn(amax, c);
+    return __fmaf_rn(__fmaf_rn(-q0, 448.0f, amax), c, q0);
+}
+
+// One 128-value block quantised to e4m3: s = RN(amax / 448) (1 for an all-zero block) and
+// codes e4m3_rne_satfinite(RN(x / s)) for |x| <= amax, x and amax bf16 values.  For
+// amax >= 2^-100 the quotients are div_by_scale's with the hardware's approximate
+// reciprocal, taken in pairs by packed fp32x2 operations: they can miss RN(x / s) by an
+// ulp, but never where that changes the e4m3 code (checked exhaustively over every bf16 x
+// and amax; code differences appear only for amax < 2^-104).  Smaller blocks divide
+// correctly rounded.  The scale is always the correctly rounded quotient (amax * RN(1 /
+// 448) alone differs from it for about half the bf16 values of amax).
+struct E4m3Block {
+    float s, yn;  // the scale and minus its approximate reciprocal
+    bool fast;
+    __device__ __forceinline__ explicit E4m3Block(float amax) {
+        fast = amax >= 0x1p-100f;
+        if (fast) s = scale_of_amax(amax);
+        else s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        yn = -rcp_approx(s);
+    }
+    // Codes of four values, the first in the low byte.  The fast path carries the quotient
+    // negated: n = x * (-y) = -q0, r = fma(n, s, x) = x - q0 * s, fma(r, -y, n) =
+    // -RN(q0 + r * y); with that arrangement a zero quotient comes out with the sign
+    // opposite to x's, so flipping the sign bit of each code (e4m3 is sign-magnitude and
+    // its rounding symmetric) gives the codes of the quotients themselves, signed zeros
+    // included.
+    __device__ __forceinline__ uint32_t codes4(float a, float b, float c, float d) const {
+        if (fast) {
+            float n0, n1, n2, n3, r0, r1, r2, r3;
+            mul2(n0, n1, a, b, yn, yn);
+            mul2(n2, n3, c, d, yn, yn);
+            fma2x(r0, r1, n0, n1, s, s, a, b);
+            fma2x(r2, r3, n2, n3, s, s, c, d);
+            fma2x(n0, n1, r0, r1, yn, yn, n0, n1);
+            fma2x(n2, n3, r2, r3, yn, yn, n2, n3);
+            return (e4m3x2(n0, n1) | (e4m3x2(n2, n3) << 16)) ^ 0x80808080u;
+        }
+        return e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s)) |
+               (e4m3x2(__fdiv_rn(c, s), __fdiv_rn(d, s)) << 16);
+    }
+};
 
 // ------------------------------------------------------------------------------------
 // tcgen05: tensor memory, MMA, commit, loads
