@@ -90,8 +90,7 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        bf16x2_to_f32(w[i], f[2 * i], f[2 * i + 1]);
     }
 }
 
@@ -242,18 +241,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                           static_cast<int64_t>(max(slot[u], 0)) * a.slot_stride;
             }
             // RMSNorm factor of each row (rows that are not stored compute on zeros); the
-            // rows go through every step side by side, so that their latencies overlap
+            // rows go through every step side by side, so that their latencies overlap.  The
+            // nope values are unpacked to fp32 once and kept for the normalisation.
+            float f[U][NC][8];
             float inv[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
                 for (int j = 0; j < NC; ++j) {
-                    float f[8];
-                    unpack8(nv[u][j], f);
+                    unpack8(nv[u][j], f[u][j]);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        fma2v(s0, s1, f[2 * i], f[2 * i + 1], f[2 * i], f[2 * i + 1]);
+                        fma2v(s0, s1, f[u][j][2 * i], f[u][j][2 * i + 1], f[u][j][2 * i],
+                              f[u][j][2 * i + 1]);
                 }
                 inv[u] = s0 + s1;
             }
@@ -265,49 +266,79 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = 0; u < U; ++u) inv[u] = rsqrtf(fmaf(inv[u], inv_r, a.epsilon));
             if constexpr (QUANT) {
                 // round to bf16 as the bf16 cache would, then quantise each 128-column block
-                // (16 chunks = one half-warp): s = amax / 448, q = e4m3(y / s).  The two
-                // half-warps' block maxima come from two whole-warp reductions in which the
-                // other half contributes zero.
+                // (16 chunks = one half-warp): s = amax / 448, q = e4m3(y / s).  Each step is
+                // taken for every block of both rows before the next, so that the latencies of
+                // the reductions and reciprocals overlap.  The two half-warps' block maxima
+                // come from two whole-warp reductions in which the other half contributes zero.
+                float y[U][NC][8];
+                uint32_t mlo[U][NC], mhi[U][NC];
 #pragma unroll
-                for (int j = 0; j < NC; ++j) {
-                    const int c = lane + 32 * j;
-                    float y[U][8];
-                    uint32_t mlo[U], mhi[U];
+                for (int u = 0; u < U; ++u)
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        float f[8];
-                        unpack8(nv[u][j], f);
-                        float m = 0.0f;
+                    for (int j = 0; j < NC; ++j) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             float g0, g1, y0, y1;
                             mul2(g0, g1, gr[j][2 * i], gr[j][2 * i + 1], inv[u], inv[u]);
-                            mul2(y0, y1, f[2 * i], f[2 * i + 1], g0, g1);
+                            mul2(y0, y1, f[u][j][2 * i], f[u][j][2 * i + 1], g0, g1);
                             const uint32_t pk = pack_bf16x2(y0, y1);
-                            y[u][2 * i] = __uint_as_float(pk << 16);
-                            y[u][2 * i + 1] = __uint_as_float(pk & 0xFFFF0000u);
-                            m = fmaxf(m, fmaxf(fabsf(y[u][2 * i]), fabsf(y[u][2 * i + 1])));
+                            bf16x2_to_f32(pk, y[u][j][2 * i], y[u][j][2 * i + 1]);
                         }
+                        const float m = fmax3_abs(fmax3_abs(y[u][j][0], y[u][j][1], y[u][j][2]),
+                                                  fmax3_abs(y[u][j][3], y[u][j][4], y[u][j][5]),
+                                                  fmax3_abs(y[u][j][6], y[u][j][7], 0.0f));
                         const uint32_t mb = __float_as_uint(m);
-                        mlo[u] = lane < 16 ? mb : 0u;
-                        mhi[u] = lane < 16 ? 0u : mb;
+                        mlo[u][j] = lane < 16 ? mb : 0u;
+                        mhi[u][j] = lane < 16 ? 0u : mb;
                     }
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        mlo[u] = warp_max_u32(mlo[u]);
-                        mhi[u] = warp_max_u32(mhi[u]);
-                    }
+                for (int u = 0; u < U; ++u)
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const E4m3Block qb(__uint_as_float(lane < 16 ? mlo[u] : mhi[u]));
-                        const uint32_t lo = qb.codes4(y[u][0], y[u][1], y[u][2], y[u][3]);
-                        const uint32_t hi = qb.codes4(y[u][4], y[u][5], y[u][6], y[u][7]);
-                        if (ok[u] && c < nope_chunks) {
-                            uint8_t* dstq = a.qcache_layer + doff[u];
-                            *reinterpret_cast<uint2*>(dstq + c * 8) = make_uint2(lo, hi);
-                            if ((lane & 15) == 0)
-                                *reinterpret_cast<float*>(dstq + R + 2 * P + 4 * (c / 16)) = qb.s;
+                    for (int j = 0; j < NC; ++j) {
+                        mlo[u][j] = warp_max_u32(mlo[u][j]);
+                        mhi[u][j] = warp_max_u32(mhi[u][j]);
+                    }
+                E4m3Block qb[U][NC];
+                bool fast = true;
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int j = 0; j < NC; ++j) {
+                        qb[u][j] = E4m3Block(__uint_as_float(lane < 16 ? mlo[u][j] : mhi[u][j]));
+                        fast = fast && qb[u][j].fast;
+                    }
+                // one warp-uniform choice: every block in the fast range (the rule) or not
+                uint32_t lo[U][NC], hi[U][NC];
+                if (__all_sync(0xffffffffu, fast)) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+#pragma unroll
+                        for (int j = 0; j < NC; ++j) {
+                            const float* v = y[u][j];
+                            lo[u][j] = qb[u][j].codes4_fast(v[0], v[1], v[2], v[3]);
+                            hi[u][j] = qb[u][j].codes4_fast(v[4], v[5], v[6], v[7]);
                         }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+#pragma unroll
+                        for (int j = 0; j < NC; ++j) {
+                            const float* v = y[u][j];
+                            lo[u][j] = qb[u][j].codes4(v[0], v[1], v[2], v[3]);
+                            hi[u][j] = qb[u][j].codes4(v[4], v[5], v[6], v[7]);
+                        }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (!ok[u]) continue;
+                    uint8_t* dstq = a.qcache_layer + doff[u];
+#pragma unroll
+                    for (int j = 0; j < NC; ++j) {
+                        const int c = lane + 32 * j;
+                        if (c >= nope_chunks) break;
+                        *reinterpret_cast<uint2*>(dstq + c * 8) = make_uint2(lo[u][j], hi[u][j]);
+                        if ((lane & 15) == 0)
+                            *reinterpret_cast<float*>(dstq + R + 2 * P + 4 * (c / 16)) = qb[u][j].s;
                     }
                 }
             } else {
@@ -319,14 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < NC; ++j) {
                         const int c = lane + 32 * j;
                         if (c >= nope_chunks) break;
-                        float f[8];
-                        unpack8(nv[u][j], f);
                         uint32_t o[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             float g0, g1, y0, y1;
                             mul2(g0, g1, gr[j][2 * i], gr[j][2 * i + 1], inv[u], inv[u]);
-                            mul2(y0, y1, f[2 * i], f[2 * i + 1], g0, g1);
+                            mul2(y0, y1, f[u][j][2 * i], f[u][j][2 * i + 1], g0, g1);
                             o[i] = pack_bf16x2(y0, y1);
                         }
                         st_v4(dst + c * 8, make_uint4(o[0], o[1], o[2], o[3]));

@@ -533,6 +533,25 @@ __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
     return r;
 }
 
+// The two bf16 halves of a packed word as fp32 values (exact): each half plus -0.0 by the
+// mixed-precision add (bf16 operand, fp32 result), which keeps the sign of a zero and
+// leaves the integer/logic pipe to other work.
+__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, 0f80000000;\n\t"
+        "add.rn.f32.bf16 %1, h, 0f80000000;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w));
+}
+
+// max(|a|, |b|, |c|) in one instruction.
+__device__ __forceinline__ float fmax3_abs(float a, float b, float c) {
+    float r;
+    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Two fp32 values to e4m3 (round to nearest even, saturating to +-448); lo in the low byte.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     uint16_t r;
@@ -621,29 +640,32 @@ __device__ __forceinline__ float scale_of_amax(float amax) {
 struct E4m3Block {
     float s, yn;  // the scale and minus its approximate reciprocal
     bool fast;
+    E4m3Block() = default;
     __device__ __forceinline__ explicit E4m3Block(float amax) {
         fast = amax >= 0x1p-100f;
         if (fast) s = scale_of_amax(amax);
         else s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
         yn = -rcp_approx(s);
     }
-    // Codes of four values, the first in the low byte.  The fast path carries the quotient
-    // negated: n = x * (-y) = -q0, r = fma(n, s, x) = x - q0 * s, fma(r, -y, n) =
+    // Codes of four values, the first in the low byte, when `fast` holds.  The quotient is
+    // carried negated: n = x * (-y) = -q0, r = fma(n, s, x) = x - q0 * s, fma(r, -y, n) =
     // -RN(q0 + r * y); with that arrangement a zero quotient comes out with the sign
     // opposite to x's, so flipping the sign bit of each code (e4m3 is sign-magnitude and
     // its rounding symmetric) gives the codes of the quotients themselves, signed zeros
     // included.
+    __device__ __forceinline__ uint32_t codes4_fast(float a, float b, float c, float d) const {
+        float n0, n1, n2, n3, r0, r1, r2, r3;
+        mul2(n0, n1, a, b, yn, yn);
+        mul2(n2, n3, c, d, yn, yn);
+        fma2x(r0, r1, n0, n1, s, s, a, b);
+        fma2x(r2, r3, n2, n3, s, s, c, d);
+        fma2x(n0, n1, r0, r1, yn, yn, n0, n1);
+        fma2x(n2, n3, r2, r3, yn, yn, n2, n3);
+        return (e4m3x2(n0, n1) | (e4m3x2(n2, n3) << 16)) ^ 0x80808080u;
+    }
+    // Codes of four values in every case.
     __device__ __forceinline__ uint32_t codes4(float a, float b, float c, float d) const {
-        if (fast) {
-            float n0, n1, n2, n3, r0, r1, r2, r3;
-            mul2(n0, n1, a, b, yn, yn);
-            mul2(n2, n3, c, d, yn, yn);
-            fma2x(r0, r1, n0, n1, s, s, a, b);
-            fma2x(r2, r3, n2, n3, s, s, c, d);
-            fma2x(n0, n1, r0, r1, yn, yn, n0, n1);
-            fma2x(n2, n3, r2, r3, yn, yn, n2, n3);
-            return (e4m3x2(n0, n1) | (e4m3x2(n2, n3) << 16)) ^ 0x80808080u;
-        }
+        if (fast) return codes4_fast(a, b, c, d);
         return e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s)) |
                (e4m3x2(__fdiv_rn(c, s), __fdiv_rn(d, s)) << 16);
     }
