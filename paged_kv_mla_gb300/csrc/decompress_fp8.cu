@@ -84,23 +84,31 @@ __global__ void __launch_bounds__(256)
             float f[16];
             const uint32_t w[8] = {nv[u][0].x, nv[u][0].y, nv[u][0].z, nv[u][0].w,
                                    nv[u][1].x, nv[u][1].y, nv[u][1].z, nv[u][1].w};
-            float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                f[2 * i] = __uint_as_float(w[i] << 16);
-                f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-                amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
-            }
+            for (int i = 0; i < 8; ++i) bf16x2_to_f32(w[i], f[2 * i], f[2 * i + 1]);
+            float amax = fmax3_abs(fmax3_abs(f[0], f[1], f[2]), fmax3_abs(f[3], f[4], f[5]),
+                                   fmax3_abs(f[6], f[7], f[8]));
+            amax = fmax3_abs(amax, fmax3_abs(f[9], f[10], f[11]), fmax3_abs(f[12], f[13], f[14]));
+            amax = fmax3_abs(amax, f[15], 0.0f);
 #pragma unroll
             for (int sh = 4; sh >= 1; sh >>= 1)  // the eight lanes of one block
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
             const E4m3Block qb(amax);
             const float s = qb.s;
+            // one warp-uniform choice of the quotient path (every block in the fast range
+            // is the rule); lanes without columns take no part in it
+            const bool all_fast = __all_sync(0xffffffffu, qb.fast || !nope);
             if (!nope) continue;
             uint32_t o[4];
+            if (all_fast) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                o[i] = qb.codes4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+                for (int i = 0; i < 4; ++i)
+                    o[i] = qb.codes4_fast(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = qb.codes4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+            }
             st_v4(x.q_latent + r * R + lane * 16, make_uint4(o[0], o[1], o[2], o[3]));
             if ((lane & 7) == 0) x.q_scale[r * kblocks + lane / 8] = s;
         }
