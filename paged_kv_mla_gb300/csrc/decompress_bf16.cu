@@ -202,6 +202,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---------------- MMA issuer (even CTA) ----------------
         if (leader && lane == 0) {
             const uint32_t idesc = idesc_bf16(256, bn, false, false);
+            // operand descriptors built once; each MMA adds its offset (16-byte units): a
+            // per-MMA rebuild sits between consecutive MMA issues and leaves the tensor
+            // pipe idle
+            const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA), 16, KB * 1024);
+            const uint64_t b_desc0 = sdesc_sw128(smem_u32(sB), 16, 1024);
             uint32_t tile_i = 0, seg = 0;
             RingPos rp;
             int64_t cur_m = -1;
@@ -228,13 +233,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(sA + kb * 1024);
-                    const uint32_t b_addr = smem_u32(sB + s * kBStageBytes);
+                    const uint64_t ad = desc_add_bytes(a_desc0, static_cast<uint32_t>(kb) * 1024);
+                    const uint64_t bd = desc_add_bytes(b_desc0, s * kBStageBytes);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_bf16_pair(d, sdesc_sw128(a_addr + k * 32, 16, KB * 1024),
-                                      sdesc_sw128(b_addr + k * 32, 16, 1024), idesc,
-                                      (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k)  // K = 16 bf16 = 32 bytes a step
+                        mma_bf16_pair(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
                     mma_commit_pair(&bars->b_empty[s], 3);
                     rp.next(kStages);
                 }

@@ -323,6 +323,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (leader && lane == 0) {
             const uint32_t idesc = idesc_e4m3(256, kBN);
+            // operand descriptors built once; each MMA adds its offset (16-byte units)
+            const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA), 16, 1024);
+            const uint64_t b_desc0 = sdesc_sw128(smem_u32(sB), 16, 1024);
             uint32_t tile_i = 0, seg = 0;
             RingPos rp;
             int64_t cur_m = -1;
@@ -345,16 +348,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     !mbar_wait(&bars->t_drained, (tile_i & 1) ^ 1, wc))
                     break;
                 tc_fence_after();
-                const uint32_t b_stage = smem_u32(sB + s * kBStageBytes);
+                const uint64_t b_stage = desc_add_bytes(b_desc0, s * kBStageBytes);
                 for (int kb = 0; kb < KB; ++kb) {
-                    const uint32_t a_addr = smem_u32(sA + kb * kABlockBytes);
-                    const uint32_t b_addr = b_stage + kb * kBKBlockBytes;
+                    const uint64_t ad = desc_add_bytes(a_desc0, static_cast<uint32_t>(kb) * kABlockBytes);
+                    const uint64_t bd = desc_add_bytes(b_stage, static_cast<uint32_t>(kb) * kBKBlockBytes);
                     const uint32_t d = tmem + static_cast<uint32_t>(kb) * kBN;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_e4m3_pair(d, sdesc_sw128(a_addr + k * 32, 16, 1024),
-                                      sdesc_sw128(b_addr + k * 32, 16, 1024), idesc,
-                                      k != 0 ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k)  // K = 32 e4m3 = 32 bytes a step
+                        mma_e4m3_pair(d, ad + 2 * k, bd + 2 * k, idesc, k != 0 ? 1u : 0u);
                     mma_commit_pair(&bars->t_full[kb], 3);
                 }
                 mma_commit_pair(&bars->b_empty[s], 3);

@@ -143,6 +143,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (leader && lane == 0) {
             const uint32_t idesc = idesc_bf16(256, bn, false, true);
+            // operand descriptors built once; each MMA adds its offset (16-byte units)
+            const uint64_t a_desc0 = sdesc_sw128(smem_u32(sStages), 16, 1024);
+            const uint64_t b_desc0 = sdesc_sw128(smem_u32(sStages + kAStageBytes), 8192, 1024);
             uint32_t tile_i = 0;
             RingPos rp;
             bool ok = true;
@@ -158,13 +161,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(sStages + s * kStageBytes);
-                    const uint32_t b_addr = a_addr + kAStageBytes;
+                    const uint64_t ad = desc_add_bytes(a_desc0, s * kStageBytes);
+                    const uint64_t bd = desc_add_bytes(b_desc0, s * kStageBytes);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_bf16_pair(d, sdesc_sw128(a_addr + k * 32, 16, 1024),
-                                      sdesc_sw128(b_addr + k * 2048, 8192, 1024), idesc,
-                                      (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k)  // K = 16: 32 bytes of A, 2048 of MN-major B
+                        mma_bf16_pair(d, ad + 2 * k, bd + 128 * k, idesc, (kb | k) != 0 ? 1u : 0u);
                     mma_commit_pair(&bars->empty[s], 3);
                     rp.next(kStages);
                 }

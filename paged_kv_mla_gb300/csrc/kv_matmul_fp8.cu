@@ -226,6 +226,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (leader && lane == 0) {
             const uint32_t idesc = idesc_e4m3(256, kBN);
+            // operand descriptors built once; each MMA adds its offset (16-byte units)
+            const uint64_t a_desc0 = sdesc_sw128(smem_u32(sStages), 16, 1024);
+            const uint64_t b_desc0 = sdesc_sw128(smem_u32(sStages + kABytes), 16, 1024);
             RingPos rp;
             uint32_t kbg = 0;  // k-blocks issued so far: accumulator kbg % kAcc
             bool ok = true;
@@ -239,14 +242,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(sStages + s * kStageBytes);
-                    const uint32_t b_addr = a_addr + kABytes;
+                    const uint64_t ad = desc_add_bytes(a_desc0, s * kStageBytes);
+                    const uint64_t bd = desc_add_bytes(b_desc0, s * kStageBytes);
                     const uint32_t d = tmem + acc * kBN;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_e4m3_pair(d, sdesc_sw128(a_addr + k * 32, 16, 1024),
-                                      sdesc_sw128(b_addr + k * 32, 16, 1024), idesc,
-                                      k != 0 ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k)  // K = 32 e4m3 = 32 bytes a step
+                        mma_e4m3_pair(d, ad + 2 * k, bd + 2 * k, idesc, k != 0 ? 1u : 0u);
                     mma_commit_pair(&bars->t_full[acc], 3);
                     mma_commit_pair(&bars->empty[s], 3);
                     rp.next(kStages);
