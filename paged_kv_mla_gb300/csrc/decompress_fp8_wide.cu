@@ -23,7 +23,10 @@
 // warp rounds its sums to bf16 into its 128-byte-swizzled 32 x 64 part of a 64 KB shared
 // box, and a store thread writes the CTA's whole 128 x 256 tile with one 3-D TMA store
 // (rows past buffer_length are clipped by the tensor map); a row block with rows that must
-// stay untouched is stored row by row by the epilogue warps instead.
+// stay untouched is stored row by row by the epilogue warps instead.  Each warp makes its
+// box writes visible to the TMA store (proxy fence, then its arrival) only after it has
+// handed back the next tile's first accumulator, so the wait for its stores to land is
+// off the MMAs' path.
 #include "pkm_device.cuh"
 #include "pkm_internal.h"
 
@@ -342,6 +345,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float ws[kKBMax];
         if (t_begin < t_end) load_ws(nn, ws);
         bool ok = true;
+        bool stage_pending = false;  // the previous tile's box awaits its fence and arrival
         for (int t = static_cast<int>(t_begin); t < t_last && ok; ++t) {
             const bool v_tile = nn >= a.n_tiles_k;
             const int n = v_tile ? nn - a.n_tiles_k : nn;
@@ -383,6 +387,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         __syncwarp();
                         if (lane == 0)
                             mbar_arrive_remote(t_empty_leader + slot * sizeof(uint64_t));
+                        if (stage_pending) {
+                            // the previous tile's box: its shared-memory writes are made
+                            // visible to the TMA store only now, after this hand-off, so
+                            // that waiting for them does not delay the MMAs
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&bars->staged);
+                            stage_pending = false;
+                        }
                     }
 #pragma unroll
                     for (int j = 0; j < 16; j += 2)
@@ -409,7 +422,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                              pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]),
                              pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
             if (blk_ok) {
-                fence_proxy_async_smem();  // the box's writes before the TMA engine reads it
+                stage_pending = true;  // fence and arrival after the next tile's first hand-off
             } else if (row0 < a.buffer_length) {
                 // a block with rows that must stay untouched: this warp writes its valid rows
                 __syncwarp();
@@ -424,11 +437,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if ((valid >> r) & 1u) st_v4(dst + r * pitch + chunk * 8, v);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->staged);
+            if (!stage_pending) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->staged);
+            }
             ++tile_i;
             nn = n_next;
             if (nn == 0) ++m;
+        }
+        if (stage_pending) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->staged);
         }
     }
 
