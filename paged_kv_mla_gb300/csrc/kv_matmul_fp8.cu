@@ -367,7 +367,8 @@ cudaError_t launch_kv_matmul_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_
                                  cudaStream_t stream) {
     const int slices = (args.k_in + 511) / 512;
     int64_t bx = (static_cast<int64_t>(args.total_rows) + 8 * kQuantUnroll - 1) / (8 * kQuantUnroll);
-    const int64_t cap = (static_cast<int64_t>(num_sms) * 8 + slices - 1) / slices;  // 8 blocks an SM
+    // one wave: four 256-thread blocks an SM are resident at the kernel's register count
+    const int64_t cap = (static_cast<int64_t>(num_sms) * 4 + slices - 1) / slices;
     if (bx > cap) bx = cap;
     if (bx < 1) bx = 1;
     fp8_quantize_rows_kernel<<<dim3(static_cast<unsigned>(bx), static_cast<unsigned>(slices)), 256,
