@@ -360,7 +360,7 @@ pkm_status mla_cache_write_paged_qcache(const void* latent, const uint32_t* inpu
                                         int32_t* dev_status, void* stream);
 
 /*
- * FP8 decompress for callers that cannot allocate device memory.  The paper has no
+ * FP8 decompress for callers that cannot allocate device memory.  The API pages have no
  * counterpart: this entry point exists for users of this library, not for the method.
  *
  * Some callers cannot call cudaMalloc or an allocator of their own: a plug-in inside an
