@@ -37,8 +37,9 @@ namespace {
 // 1. gather + quantise
 // ------------------------------------------------------------------------------------
 
-// One warp per output row, two rows at a time: the rows are resolved and all their loads
-// issued before any arithmetic.  A lane holds 16 nope values (32 bytes), so a 128-column
+// Each warp takes a contiguous range of output rows, two at a time, resolving them with a
+// forward walk (one binary search per warp, page ids reused along a page): the rows are
+// resolved and all their loads issued before any arithmetic.  A lane holds 16 nope values (32 bytes), so a 128-column
 // block is eight lanes (kv_lora_rank <= 512 fits one pass); lanes below rope_dim / 8 also
 // carry one 16-byte chunk of the rope columns.
 constexpr int kGatherRows = 2;
@@ -55,13 +56,17 @@ __global__ void __launch_bounds__(256)
     const int kblocks = R / 128;
     const bool nope = lane * 16 < R;
     const bool rope = lane < (C - R) / 8;
-    for (int64_t r0 = warp_id; r0 < row_end; r0 += kGatherRows * nwarps) {
+    // this warp's rows: a contiguous range, resolved by a forward walk
+    const int64_t rb = row_end * warp_id / nwarps;
+    const int64_t re = row_end * (warp_id + 1) / nwarps;
+    RowSourceWalk walk(a, rb);
+    for (int64_t r0 = rb; r0 < re; r0 += kGatherRows) {
         int64_t off[kGatherRows];
         uint4 nv[kGatherRows][2], rv[kGatherRows];
 #pragma unroll
         for (int u = 0; u < kGatherRows; ++u) {
-            const int64_t r = r0 + u * nwarps;
-            off[u] = decompress_row_source(a, r, row_end);  // -1 past row_end too
+            const int64_t r = r0 + u;
+            off[u] = r < re ? walk.source(a, r) : -1;
             const uint16_t* src = a.cache_layer + (off[u] >= 0 ? off[u] : 0);
             const bool live = off[u] >= 0;
             nv[u][0] = live && nope ? ld_nc_v4(src + lane * 16) : make_uint4(0u, 0u, 0u, 0u);
@@ -74,7 +79,7 @@ __global__ void __launch_bounds__(256)
                 if (off[u] == -2 && lane == 0) report(a.status, PKM_ERR_OUT_OF_RANGE);
                 continue;
             }
-            const int64_t r = r0 + u * nwarps;
+            const int64_t r = r0 + u;
             uint16_t* lat = a.k_latent + r * C;
             if (nope) {
                 st_v4(lat + lane * 16, nv[u][0]);

@@ -178,6 +178,56 @@ __device__ __forceinline__ int64_t decompress_row_source(const DecompressArgs& a
     return decompress_row_locate(a, r, row_end, &page, &slot);
 }
 
+// decompress_row_source for a run of increasing rows: one binary search for the first row,
+// then the request only moves forward and the page id of the last logical page is reused,
+// so a row costs no chain of dependent loads.  Same results as decompress_row_source.
+struct RowSourceWalk {
+    int b;
+    int64_t lo, hi;        // request b covers rows [lo, hi)
+    uint64_t co;           // cache_offsets[b]
+    uint64_t page_key;     // (b, logical page) whose id is in page
+    uint32_t page;
+
+    __device__ __forceinline__ RowSourceWalk(const DecompressArgs& a, int64_t r) {
+        const uint32_t* bro = a.row_offsets;
+        int l = 0, h = a.batch;  // largest b with bro[b] <= r (0 when r < bro[0])
+        while (h - l > 1) {
+            const int mid = (l + h) >> 1;
+            if (static_cast<int64_t>(__ldg(bro + mid)) <= r) l = mid;
+            else h = mid;
+        }
+        b = l;
+        lo = __ldg(bro + l);
+        hi = __ldg(bro + l + 1);
+        co = __ldg(a.cache_offsets + l);
+        page_key = ~0ull;
+        page = 0;
+    }
+
+    // Rows must come in non-decreasing order.
+    __device__ __forceinline__ int64_t source(const DecompressArgs& a, int64_t r) {
+        while (r >= hi && b + 1 < a.batch) {
+            ++b;
+            lo = hi;
+            hi = __ldg(a.row_offsets + b + 1);
+            co = __ldg(a.cache_offsets + b);
+        }
+        if (r < lo || r >= hi) return -1;
+        const uint64_t t = co + static_cast<uint64_t>(r - lo);
+        const uint64_t lp = t / static_cast<uint64_t>(a.page_size);
+        if (lp >= static_cast<uint64_t>(a.max_pages)) return -2;
+        const uint64_t key = (static_cast<uint64_t>(b) << 32) | lp;
+        if (key != page_key) {
+            page = __ldg(a.page_table + static_cast<int64_t>(b) * a.max_pages + lp);
+            page_key = key;
+        }
+        if (page >= static_cast<uint32_t>(a.num_pages)) return -2;
+        const uint64_t slot = t - lp * static_cast<uint64_t>(a.page_size);
+        return static_cast<int64_t>(page) * a.page_stride +
+               static_cast<int64_t>(slot) * a.slot_stride;
+    }
+};
+
 // min(buffer_length, row_offsets[batch]): rows at or past it are not written.
 __device__ __forceinline__ int64_t decompress_row_end(const DecompressArgs& a) {
     const int64_t covered = static_cast<int64_t>(__ldg(a.row_offsets + a.batch));
