@@ -229,6 +229,22 @@ def test_fp8_decompress_edges():
     check_full_fp8(d, expect_status=4)
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_leading_rows_and_empty_requests_are_untouched(fp8):
+    """buffer_row_offsets starting above zero (generic_flare_mla_decompress_k_cache_ragged_paged,
+    Args buffer_row_offsets_1d: rows below the first offset belong to no request) with empty
+    requests between full ones and a request ending mid-page: the leading rows and every
+    uncovered row stay untouched, the others match the oracle."""
+    d = workloads.make_decompress("lead", 421, [90, 0, 170, 0, 0, 33], [5, 0, 31, 0, 0, 7], 32,
+                                  512, 64, 512, fp8=fp8)
+    d.buffer_row_offsets = (d.buffer_row_offsets + 37).astype(np.uint32)
+    d.buffer_length = int(d.buffer_row_offsets[-1]) + 11
+    if fp8:
+        check_full_fp8(d)
+    else:
+        check_full_decompress(d)
+
+
 def test_deepseek_v3_fp8_decompress_full_size():
     d = workloads.WORKLOADS["deepseek_v3_fp8_decompress"]()
     g = DeviceDecompress(d, fp8=True)
