@@ -58,6 +58,7 @@ def test_tiny_decompress():
     (128, 64, 384, 128, [1000, 77], [31, 5], 1),                          # bn = 128
     (256, 0, 320, 64, [250, 3, 190], [0, 0, 17], 1),                      # bn = 64, no rope
     (64, 16, 256, 4, [40, 90, 1], [3, 0, 0], 3),                          # tiny pages
+    (192, 64, 256, 32, [600, 45, 211], [0, 3, 9], 1),                     # odd k-block count
 ])
 def test_decompress_mid(R, P, N, ps, lengths, offsets, layers):
     d = workloads.make_decompress("mid", 200 + R + N, lengths, offsets, ps, R, P, N,
