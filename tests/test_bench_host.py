@@ -59,3 +59,23 @@ def test_oracle_pool_covers_each_row_once():
         assert rows == 4
     finally:
         pool.close()
+
+
+def test_roofline_rows_recompute_from_their_own_fields():
+    """Each bench row's roofline object is recomputable from the fields it carries: the
+    bound is the slower of FLOPs at the tensor peak and algorithmic bytes at the HBM peak,
+    `achieved` is that unit's rate over the row's device time and `frac` = achieved / peak."""
+    import bench
+    peaks = {"hbm_gbs": 6775.3}
+    # a tensor-bound row (the bf16 decompress shape) and an HBM-bound row (a cache write)
+    for flop, nbytes, t in [(4.486e14, 9.545e8, 2.64e-4), (0.0, 1.456e8, 4.1e-5),
+                            (4.486e14, 9.47e8, 2.65e-4)]:
+        r = bench.roofline_row(["k"], t, flop, nbytes, peaks, 1933.3, "measured burst")
+        t_tensor = flop / (1933.3e12) if flop else 0.0
+        t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+        assert r["bound"] == ("tensor" if t_tensor >= t_hbm else "hbm")
+        rate = flop / r["ms"] * 1e3 / 1e12 if r["bound"] == "tensor" else nbytes / r["ms"] * 1e3 / 1e9
+        assert abs(r["achieved"] - rate) <= 1e-9 * rate
+        assert abs(r["frac"] - r["achieved"] / r["peak"]) <= 1e-12
+        assert r["unit"] == ("TFLOP/s" if r["bound"] == "tensor" else "GB/s")
+        assert abs(r["hbm_frac"] - nbytes / t / 1e9 / peaks["hbm_gbs"]) <= 1e-12
